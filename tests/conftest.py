@@ -1,0 +1,25 @@
+"""Shared pytest configuration.
+
+Markers:
+  gpu  -- needs a CUDA device (sm_103a); parity tests of the CUDA path against
+          the CPU oracle.  Everything unmarked runs on a CPU-only machine.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
+
+
+@pytest.fixture(scope="session")
+def oracle():
+    import oracle as _oracle
+    _oracle.build()
+    return _oracle
