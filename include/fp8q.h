@@ -1,0 +1,207 @@
+/*
+ * fp8q.h -- C ABI of libfp8q: fine-grained FP8 (E4M3) quantisation and the
+ * per-group-scaled FP8 GEMM on one sm_103a GPU.
+ *
+ * The operations follow the FP8 training recipe of DeepSeek-V3 as described
+ * on these pages:
+ *   - dssusan.co.kr board post 91437 (an excerpt of the DeepSeek-V3 report's
+ *     FP8 section): paragraph 1 (power-of-two scaling factors for some
+ *     activations), paragraph 2 (max-abs computed online per 1x128 activation
+ *     tile and per 128x128 weight block; the scaling factor follows from it),
+ *     paragraph 3 (Figure 6: per-group scaling factors along the GEMM's inner
+ *     dimension K, applied as dequantisation, FP32 accumulation), paragraph 4
+ *     (Figure 7 (a): 1x128 per token per 128 channels, 128x128 per 128 input
+ *     by 128 output channels; 1x128 tiles become 128x1 tiles in the backward
+ *     pass);
+ *   - "Deepseek - Not For everyone" (xn--jj0bz6z98ct0a29q.com post 278251),
+ *     paragraph 4: the max-abs is mapped onto the largest finite FP8 value;
+ *   - youlimart.com FAQ post 597629, paragraph 2 (Figure 6): Fprop, Dgrad and
+ *     Wgrad all run in FP8, taking FP8 inputs and producing BF16 or FP32;
+ *   - "FP8 mixed precision -- где и как DeepSeek снизили точность
+ *     вычислений?" (Data Science by ODS.ai): E4M3 for every tensor, FP32
+ *     accumulation of the tensor-core partial sums.
+ *
+ * Conventions for every call:
+ *   - Tensors are row-major; every leading dimension (ld*) is in ELEMENTS of
+ *     that tensor's type.  E4M3 tensors are raw bytes (1 byte per element),
+ *     BF16 tensors raw 16-bit patterns.
+ *   - All pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates or frees device memory, and keeps no pointer after a call
+ *     returns.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).
+ *   - E4M3 means the OCP "E4M3FN" encoding (bias 7, largest finite 448, NaN
+ *     0x7F/0xFF, no infinity).  Values are rounded to nearest-even and
+ *     saturated to +-448.
+ *   - Scales s are FP32 with dequantised value = decode(q) * s.  For a group
+ *     with max-abs value amax, a = max(amax, 2^-116) and
+ *       FP8Q_SCALE_FP32: s = a / 448, codes E4M3(x * (448 / a)), both FP32
+ *                        divisions rounded to nearest;
+ *       FP8Q_SCALE_POW2: s = 2^e, e the smallest integer with 448 * 2^e >= a,
+ *                        codes E4M3(x * 2^-e).
+ *     Inputs must be finite; NaN/Inf inputs give unspecified codes.
+ *   - Argument errors are returned synchronously and nothing is launched.
+ *     A device-side failure (a bounded wait that gave up) is recorded in a
+ *     device status word and returned by fp8q_sync_status().
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8q_status {
+  FP8Q_OK = 0,
+  FP8Q_ERR_INVALID = 1,     /* null pointer where one is required, unknown enum */
+  FP8Q_ERR_SHAPE = 2,       /* negative size, K/T not a multiple of 128, ld too small */
+  FP8Q_ERR_ALIGN = 3,       /* pointer or leading dimension breaks a 16-byte rule */
+  FP8Q_ERR_UNSUPPORTED = 4, /* current device is not sm_103, or too little shared memory */
+  FP8Q_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  FP8Q_ERR_TIMEOUT = 6      /* a device-side wait gave up (reported by fp8q_sync_status) */
+} fp8q_status;
+
+enum { FP8Q_SCALE_FP32 = 0, FP8Q_SCALE_POW2 = 1 };
+enum { FP8Q_OUT_BF16 = 0, FP8Q_OUT_FP32 = 1 };
+/* Layout of the B-operand scales of fp8q_gemm. */
+enum {
+  FP8Q_BSCALE_BLOCK = 0,   /* one per 128x128 block:  sb[(n/128) * ld_sb + k/128] */
+  FP8Q_BSCALE_BLOCK_T = 1, /* one per 128x128 block, grid transposed:
+                              sb[(k/128) * ld_sb + n/128] (Dgrad reading a weight's grid) */
+  FP8Q_BSCALE_ROW = 2      /* one per row n per 128-K group (128x1 tiles, Wgrad):
+                              sb[(k/128) * ld_sb + n] */
+};
+
+/*
+ * Activation quantisation, 1x128 tiles: one scale per row (token) m per 128
+ * columns (channels) ([dssusan] paragraph 2 and paragraph 4, Figure 7 (a)(1)).
+ *   x   BF16 [M][ldx], reads columns [0, K).       K % 128 == 0, M >= 0.
+ *   q   E4M3 [M][ldq], writes columns [0, K).
+ *   sa  FP32, MN-major: scale of (m, group g) at sa[g * ld_sa + m], ld_sa >= M.
+ * Alignment: x and q 16-byte aligned, ldx % 8 == 0, ldq % 16 == 0.
+ */
+fp8q_status fp8q_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx,
+                           void *q, int64_t ldq, float *sa, int64_t ld_sa,
+                           int scale_mode, void *stream);
+
+/*
+ * Activation quantisation for the backward pass, 128x1 tiles: one scale per
+ * column (channel) c per 128 rows (tokens) ([dssusan] paragraph 4: 1x128
+ * tiles become 128x1 tiles).  The codes are written TRANSPOSED so the token
+ * dimension is contiguous, i.e. K-major for the Wgrad GEMM.
+ *   x      BF16 [T][ldx], columns [0, C).           T % 128 == 0, C % 8 == 0.
+ *   qT     E4M3 [C][ldqT], qT[c][t] = code of x[t][c].
+ *   sT     FP32, scale of (t-group tg, c) at sT[tg * ld_sT + c], ld_sT >= C.
+ *   q_rows optional (NULL to skip): the 1x128 quantisation of the same x,
+ *          computed from the same read: E4M3 [T][ldq_rows] and
+ *          s_rows[g * ld_s_rows + t] exactly as fp8q_quant_act would write
+ *          them.  Requires C % 128 == 0; s_rows must then be non-NULL.
+ * Alignment: x, qT (and q_rows) 16-byte aligned; ldx % 8, ldqT % 16,
+ * ldq_rows % 16 == 0.
+ */
+fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int64_t ldx,
+                             void *qT, int64_t ldqT, float *sT, int64_t ld_sT,
+                             void *q_rows, int64_t ldq_rows, float *s_rows,
+                             int64_t ld_s_rows, int scale_mode, void *stream);
+
+/*
+ * Weight quantisation, 128x128 blocks: one scale per 128 rows (output
+ * channels) x 128 columns (input channels) ([dssusan] paragraph 4, Figure
+ * 7 (a)(2)).  A last partial block of rows covers only the rows that exist.
+ *   w   BF16 [N][ldw], columns [0, K).              K % 128 == 0, N >= 0.
+ *   q   E4M3 [N][ldq].
+ *   qT  optional (NULL to skip): E4M3 [K][ldqT], qT[k][n] = q[n][k] -- the
+ *       K-major B operand of the Dgrad GEMM (dX = dY * W).
+ *   sb  FP32 [ceil(N/128)][ld_sb], block (nb, kb) at sb[nb * ld_sb + kb],
+ *       ld_sb >= K/128.
+ * Alignment: w, q, qT 16-byte aligned; ldw % 8, ldq % 16, ldqT % 16 == 0.
+ */
+fp8q_status fp8q_quant_weight(const void *w, int64_t N, int64_t K, int64_t ldw,
+                              void *q, int64_t ldq, void *qT, int64_t ldqT,
+                              float *sb, int64_t ld_sb, int scale_mode,
+                              void *stream);
+
+/*
+ * FP8 GEMM with per-group scaling along K ([dssusan] paragraph 3, Figure 6;
+ * [youlimart] paragraph 2):
+ *   C[m][n] = sum over 128-wide groups kb of
+ *             sa(m,kb) * sb(n,kb) * sum_{k in kb} decode(a[m][k]) * decode(b[n][k])
+ * The inner sums run on the tensor cores into an FP32 partial per group; each
+ * partial is scaled and added into an FP32 accumulator by separate warps.
+ * The result is stored as FP32, or rounded to nearest-even BF16.
+ *   a   E4M3 [M][lda] (K-major), sa FP32 at sa[kb * ld_sa + m], ld_sa >= M.
+ *   b   E4M3 [N][ldb] (K-major), sb FP32 laid out per bscale_kind (see enum).
+ *   c   [M][ldc] BF16 or FP32 per out_dtype.
+ *   K % 128 == 0; M, N >= 0 (tails are masked).  K == 0 writes zeros.
+ * Alignment: a, b, c 16-byte aligned; lda % 16 == 0, ldb % 16 == 0,
+ * ldc * sizeof(out) % 16 == 0.
+ * Fprop: a = quantised activations, b = quantised weight, BLOCK scales.
+ * Dgrad: a = quantised dY, b = the weight's qT, BLOCK_T over the weight's sb.
+ * Wgrad: a = dY's qT, b = X's qT, sa = dY's sT, sb = X's sT with ROW scales.
+ */
+fp8q_status fp8q_gemm(const void *a, int64_t lda, const float *sa,
+                      int64_t ld_sa, const void *b, int64_t ldb,
+                      const float *sb, int64_t ld_sb, int bscale_kind, void *c,
+                      int64_t ldc, int out_dtype, int64_t M, int64_t N,
+                      int64_t K, void *stream);
+
+/*
+ * Grouped FP8 GEMM for MoE experts: rows [offs[g], offs[g+1]) of A (tokens
+ * sorted by expert, top-1 routing) are multiplied by expert g's weight.
+ *   a     E4M3 [M][lda], sa at sa[kb * ld_sa + m] as in fp8q_gemm.
+ *   b     E4M3 [G][N][ldb] (expert g's rows start at b + g*N*ldb).
+ *   sb    FP32 [G][ceil(N/128)][K/128] (BLOCK layout per expert).
+ *   offs  int32 DEVICE array [G+1]: 0 <= offs[0] <= ... <= offs[G] <= M.
+ *         Empty experts are allowed.  Rows outside [offs[0], offs[G]) are
+ *         not written.  Offsets that break the ordering are clamped into
+ *         [0, M] and a decreasing step is treated as an empty expert.
+ *   c     [M][ldc] BF16 or FP32.
+ *   1 <= G <= 1024; other rules as fp8q_gemm.
+ */
+fp8q_status fp8q_grouped_gemm(const void *a, int64_t lda, const float *sa,
+                              int64_t ld_sa, const void *b, int64_t ldb,
+                              const float *sb, const int32_t *offs, int G,
+                              void *c, int64_t ldc, int out_dtype, int64_t M,
+                              int64_t N, int64_t K, void *stream);
+
+/*
+ * Plain FP32 -> E4M3 conversion of n values (round to nearest-even, saturate
+ * to +-448, NaN -> 0x7F), with no scaling.  The quantisers use the same
+ * conversion; this entry exposes it so it can be checked on every FP32 bit
+ * pattern.  x: FP32 [n], q: E4M3 [n]; both 16-byte aligned.
+ */
+fp8q_status fp8q_cast_e4m3(const float *x, int64_t n, void *q, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear this device's status word.
+ * Returns FP8Q_ERR_TIMEOUT if a kernel's bounded wait gave up since the last
+ * call, FP8Q_ERR_CUDA if synchronisation failed, else FP8Q_OK.
+ */
+fp8q_status fp8q_sync_status(void *stream);
+
+/*
+ * Set the time limit, in nanoseconds, of every device-side wait launched
+ * afterwards from this process (default 2e9 = 2 s; 0 restores the default).
+ */
+void fp8q_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Diagnostic: launch one CTA that waits, with the bounded wait the GEMM uses,
+ * on a barrier that nothing ever completes, for at most timeout_ns.  The wait
+ * must give up, record FP8Q_ERR_TIMEOUT in the status word and return; the
+ * caller then reads it with fp8q_sync_status().
+ */
+fp8q_status fp8q_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *fp8q_status_string(fp8q_status s);
+
+/* ABI version of this header (major * 100 + minor). */
+int fp8q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */
