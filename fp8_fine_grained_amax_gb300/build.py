@@ -7,8 +7,9 @@ needs no GPU driver (the symbol check in the CPU tests relies on this).
 
 The GEMM kernel gives registers from its control warpgroup to its epilogue
 warpgroups with setmaxnreg; that split is only valid if ptxas builds the
-kernel for exactly 168 registers per thread at launch.  The build reads
-ptxas' report and refuses to link a library that breaks this.
+kernel for exactly the launch register count the source assumes
+(``kLaunchRegs`` in csrc/gemm.cu).  The build reads ptxas' report and refuses
+to link a library that breaks this.
 """
 from __future__ import annotations
 
@@ -26,7 +27,6 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8q.so")
 SOURCES = ["gemm.cu", "quant.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-GEMM_LAUNCH_REGS = 168
 
 
 def nvcc() -> str:
@@ -60,17 +60,26 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, r.stderr
 
 
-def _check_gemm_registers(ptxas_log: str) -> None:
+def launch_regs_of(gemm_src: str) -> int:
+    """The per-thread launch register count the GEMM source is written for."""
+    m = re.search(r"constexpr int kLaunchRegs = (\d+);", open(gemm_src).read())
+    if not m:
+        raise RuntimeError("kLaunchRegs not found in " + gemm_src)
+    return int(m.group(1))
+
+
+def check_gemm_registers(ptxas_log: str, expected: int) -> None:
+    """Every fp8q_gemm_kernel instantiation must be built for `expected` registers."""
     entries = re.split(r"Compiling entry function", ptxas_log)
     found = 0
     for e in entries:
         if "fp8q_gemm_kernel" not in e.split("\n", 1)[0]:
             continue
         m = re.search(r"Used (\d+) registers", e)
-        if not m or int(m.group(1)) != GEMM_LAUNCH_REGS:
+        if not m or int(m.group(1)) != expected:
             raise RuntimeError(
                 "GEMM kernel not built for %d registers per thread (ptxas: %s); the "
-                "setmaxnreg split would not balance" % (GEMM_LAUNCH_REGS, m and m.group(0)))
+                "setmaxnreg split would not balance" % (expected, m and m.group(0)))
         found += 1
     if found == 0:
         raise RuntimeError("ptxas report names no fp8q_gemm_kernel")
@@ -83,7 +92,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         results = dict(zip(SOURCES, ex.map(_compile, SOURCES)))
-    _check_gemm_registers(results["gemm.cu"][1])
+    check_gemm_registers(results["gemm.cu"][1], launch_regs_of(os.path.join(CSRC, "gemm.cu")))
     if verbose:
         for src, (_, log) in results.items():
             print(f"== {src}\n{log}")

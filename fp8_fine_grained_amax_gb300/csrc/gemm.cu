@@ -19,9 +19,11 @@
 //               and to signal the partial.
 //   warps 2-3   idle (they complete the first warpgroup).
 //   warps 4-11  epilogue: tcgen05.ld the partial (each thread one row, 128
-//               columns), acc += P * sa(m,kb) * sb(n,kb) in FP32 registers,
-//               release the TMEM buffer; after the last group, store C as
-//               FP32 or round-to-nearest-even BF16.
+//               columns, 16 at a time), acc += P * sa(m,kb) * sb(n,kb) in FP32
+//               registers with packed two-lane FMAs (fma.rn.f32x2), release the
+//               TMEM buffer; after the last group, store C as FP32 or
+//               round-to-nearest-even BF16.  The scales of group kb+1 are
+//               loaded while group kb is folded.
 //
 // Registers: the kernel is built for 384 threads at 168 registers each (the
 // register file of each SM sub-partition holds three warps at 168).  The
@@ -56,11 +58,18 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 128 + kEpiWarps * 32;   // 3 warpgroups
+constexpr int kEpiWarps = 8;                     // 2 warpgroups: 4 TMEM lane quarters x 2
+constexpr int kEpiCols = BN / (kEpiWarps / 4);   // columns folded by each epilogue thread
+constexpr int kThreads = 128 + kEpiWarps * 32;   // control warpgroup + epilogue warpgroups
+constexpr int kWarpsPerSubpartition = kThreads / 128;
 constexpr int kLaunchRegs = 168;                 // must match ptxas' count (checked by the build)
 constexpr int kCtlRegs = 40, kEpiRegs = 232;
-static_assert(kCtlRegs + 2 * kEpiRegs == 3 * kLaunchRegs, "register split must balance");
+// setmaxnreg can only hand out what the launch allocated on each sub-partition
+// (one control warp and kWarpsPerSubpartition - 1 epilogue warps there)
+static_assert(kCtlRegs + (kWarpsPerSubpartition - 1) * kEpiRegs <=
+                  kWarpsPerSubpartition * kLaunchRegs,
+              "register split must fit the launch allocation");
+static_assert(kLaunchRegs * kThreads <= 65536, "launch register budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kABytes = BM * BK;
 constexpr uint32_t kBBytes = BN * BK;
@@ -236,10 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================== epilogue
     const int ew = warp - 4;
     const int quarter = warp & 3;        // TMEM lanes this warp may access
-    const int col_base = (ew >> 2) * 128;  // which half of the 256 columns
+    const int col_base = (ew >> 2) * kEpiCols;  // this warp's columns of the 256
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int NB = (p.N + 127) / 128;
+    const int et = ew * 32 + lane;  // staging slot for per-column scales (< BN stages)
     int tb = 0;
     uint32_t tphase = 0;
     uint32_t sb_iter = 0;
@@ -249,31 +259,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = tl.a_row + row_in_tile;
       const bool row_in = m < p.M;
       const int ncol0 = tl.n0 + col_base;
+      const int nb = ncol0 / 128;
       const float *sb_g = p.sb;
       if (kGrouped) sb_g += static_cast<int64_t>(tl.g) * NB * p.num_kb;
-      float acc[128];
+      // scales of K-group kb: sa of this row; sb of this warp's 128 columns
+      // (block kinds) or of column n0 + et (per-column kind, staged in smem)
+      auto load_sa = [&](int kb) {
+        return row_in ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ld_sa + m) : 0.0f;
+      };
+      auto load_sb = [&](int kb) {
+        if (kBScale == FP8Q_BSCALE_BLOCK)
+          return nb < NB ? __ldg(sb_g + static_cast<int64_t>(nb) * (kGrouped ? p.num_kb : p.ld_sb) +
+                                 kb)
+                         : 0.0f;
+        if (kBScale == FP8Q_BSCALE_BLOCK_T)
+          return nb < NB ? __ldg(p.sb + static_cast<int64_t>(kb) * p.ld_sb + nb) : 0.0f;
+        const int n = tl.n0 + et;
+        return (et < BN && n < p.N) ? __ldg(p.sb + static_cast<int64_t>(kb) * p.ld_sb + n) : 0.0f;
+      };
+      uint64_t acc[kEpiCols / 2];  // packed FP32 pairs: columns (2i, 2i+1) of this thread's
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < kEpiCols / 2; ++j) acc[j] = 0ull;
+      float sa_nx = p.num_kb > 0 ? load_sa(0) : 0.0f;
+      float sb_nx = p.num_kb > 0 ? load_sb(0) : 0.0f;
 
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        const float sa_v = row_in ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ld_sa + m) : 0.0f;
-        float scale = sa_v;
-        if (kBScale == FP8Q_BSCALE_BLOCK) {
-          const int nb = ncol0 / 128;
-          const float sbv =
-              nb < NB ? __ldg(sb_g + static_cast<int64_t>(nb) * (kGrouped ? p.num_kb : p.ld_sb) + kb)
-                      : 0.0f;
-          scale = sa_v * sbv;
-        } else if (kBScale == FP8Q_BSCALE_BLOCK_T) {
-          const int nb = ncol0 / 128;
-          const float sbv = nb < NB ? __ldg(p.sb + static_cast<int64_t>(kb) * p.ld_sb + nb) : 0.0f;
-          scale = sa_v * sbv;
-        } else {
+        // the scales of group kb were loaded one iteration ago; fetch kb+1 now
+        const float sa_v = sa_nx, sb_v = sb_nx;
+        if (kb + 1 < p.num_kb) {
+          sa_nx = load_sa(kb + 1);
+          sb_nx = load_sb(kb + 1);
+        }
+        if (kBScale == FP8Q_BSCALE_ROW) {
           // per-column scales, staged through shared memory by all 256 threads
-          const int et = ew * 32 + lane;
-          const int n = tl.n0 + et;
-          ctl->sb_row[sb_iter & 1][et] =
-              n < p.N ? __ldg(p.sb + static_cast<int64_t>(kb) * p.ld_sb + n) : 0.0f;
+          if (et < BN) ctl->sb_row[sb_iter & 1][et] = sb_v;
           mbar_arrive(smem_u32(&ctl->sbfull[sb_iter & 1]));
           // every lane waits; the warp then agrees (and reconverges) on the outcome
           const bool got = mbar_wait_bounded(smem_u32(&ctl->sbfull[sb_iter & 1]),
@@ -284,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
+        const uint64_t scale2 = pack_f32x2(sa_v * sb_v, sa_v * sb_v);
+        const uint64_t sa2 = pack_f32x2(sa_v, sa_v);
         const bool got = mbar_wait_bounded(smem_u32(&ctl->tfull[tb]), tphase, abort_flag,
                                            &g_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
         if (!__all_sync(0xffffffffu, got)) {  // tcgen05.ld below needs the whole warp
@@ -293,25 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(tb * BN + col_base);
 #pragma unroll
-        for (int ch = 0; ch < 4; ch += 2) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(taddr + ch * 32, r0);
-          tmem_ld_32x32b_x32(taddr + ch * 32 + 32, r1);
+        for (int ch = 0; ch < kEpiCols / 16; ++ch) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + ch * 16, r);
           tmem_wait_ld();
           if (kBScale == FP8Q_BSCALE_ROW) {
-            const float *sbr = &ctl->sb_row[sb_iter & 1][col_base + ch * 32];
+            const uint64_t *sbr =
+                reinterpret_cast<const uint64_t *>(&ctl->sb_row[sb_iter & 1][col_base + ch * 16]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[ch * 32 + j] = fmaf(__uint_as_float(r0[j]), sa_v * sbr[j], acc[ch * 32 + j]);
-              acc[ch * 32 + 32 + j] =
-                  fmaf(__uint_as_float(r1[j]), sa_v * sbr[32 + j], acc[ch * 32 + 32 + j]);
-            }
+            for (int j = 0; j < 8; ++j)
+              ffma2(acc[ch * 8 + j], pack_u32x2(r[2 * j], r[2 * j + 1]), fmul2(sbr[j], sa2));
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[ch * 32 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[ch * 32 + j]);
-              acc[ch * 32 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[ch * 32 + 32 + j]);
-            }
+            for (int j = 0; j < 8; ++j)
+              ffma2(acc[ch * 8 + j], pack_u32x2(r[2 * j], r[2 * j + 1]), scale2);
           }
         }
         tc_fence_before();
@@ -325,28 +341,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- store the tile row (128 columns of row m)
       if (m < tl.row_end && ncol0 < p.N) {
-        const bool full = ncol0 + 128 <= p.N;
+        const bool full = ncol0 + kEpiCols <= p.N;
         if (kOutF32) {
           float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
-          for (int j = 0; j < 128; j += 4) {
+          for (int j = 0; j < kEpiCols; j += 4) {
+            const float2 lo = unpack_f32x2(acc[j / 2]), hi = unpack_f32x2(acc[j / 2 + 1]);
             if (full || ncol0 + j + 4 <= p.N) {
-              *reinterpret_cast<float4 *>(crow + j) =
-                  make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+              *reinterpret_cast<float4 *>(crow + j) = make_float4(lo.x, lo.y, hi.x, hi.y);
             } else {
+              const float v[4] = {lo.x, lo.y, hi.x, hi.y};
               for (int e = 0; e < 4; ++e)
-                if (ncol0 + j + e < p.N) crow[j + e] = acc[j + e];
+                if (ncol0 + j + e < p.N) crow[j + e] = v[e];
             }
           }
         } else {
           __nv_bfloat16 *crow =
               static_cast<__nv_bfloat16 *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
-          for (int j = 0; j < 128; j += 8) {
+          for (int j = 0; j < kEpiCols; j += 8) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h = __floats2bfloat162_rn(acc[j + 2 * e], acc[j + 2 * e + 1]);
+              const float2 v = unpack_f32x2(acc[j / 2 + e]);
+              __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
               w[e] = *reinterpret_cast<uint32_t *>(&h);
             }
             if (full || ncol0 + j + 8 <= p.N) {
