@@ -1,21 +1,30 @@
 """Benchmark of the fine-grained FP8 hot path on GB300.
 
-One step = the whole hot path of one linear layer's forward pass on seeded
-synthetic inputs already resident in HBM:
+One step = the whole hot path of one workload on seeded synthetic inputs that
+are already resident in HBM.  The default workload is the forward pass of one
+linear layer, M=4096 tokens, N=7168 outputs, K=7168 inputs:
   quantise the activation X [M][K] (1x128 tiles), quantise the weight W [N][K]
   (128x128 blocks), FP8 GEMM with per-128-K-group scaling, BF16 output.
-Default workload: M=4096, N=7168, K=7168 (the single Fprop linear).  Other
-workloads (--workload) cover the backward pass and the MoE grouped GEMM.
+Other workloads (--workload):
+  linear_bwd_T8192       Dgrad + Wgrad of a 7168->2048 linear over 8192 tokens,
+                         with the 128x1 / fused 1x128 and 128x128 quantisers
+  moe_fprop_16x16384     MoE up- (7168->4096) and down-projection (2048->7168),
+                         16 experts, Dirichlet(0.5) top-1 routing, grouped GEMMs
+  square_<n>             n x n x n Fprop step (quantise both operands + GEMM)
+  quant_act_<t>          1x128 quantisation of t x 7168 (GB/s)
+  quant_act_pow2_<t>     same with power-of-two scales (GB/s)
+  quant_act_T_<t>        128x1 transposed quantisation of t x 7168 (GB/s)
+  quant_weight_<g>x4096  128x128 quantisation of g stacked 4096x7168 weights (GB/s)
 
-Prints ONE JSON line (rank 0).  `value` is the step's algorithmic GEMM
-FLOPs (2MNK, summed over ranks) per second of device time; the per-kernel
-figures, the roofline of the dominant kernel, an end-to-end number through
-host buffers, clocks seen during the timed region and the CPU oracle's
-throughput on a bounded sample are added to the same line.
+Prints ONE JSON line (rank 0).  `value` is the step's algorithmic work (GEMM
+FLOPs 2MNK over real rows, or quantiser bytes) summed over ranks per second of
+device time.  The per-kernel times, the roofline of the dominant kernel, an
+end-to-end number through host buffers, the clocks seen during the timed
+region and the CPU oracle's throughput on a bounded sample are added.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
-Multi-GPU runs (torchrun, one rank per GPU) are independent replicas of the
+Multi-GPU runs (torchrun, one process per GPU) are independent replicas of the
 same step (weak scaling): the path has no exchange step.
 """
 from __future__ import annotations
@@ -42,6 +51,7 @@ L2_BYTES = 126 * 1024 * 1024
 FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor-core rate
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+CSRC = os.path.join(ROOT, "fp8_fine_grained_amax_gb300", "csrc")
 
 
 # ----------------------------------------------------------------- helpers
@@ -100,7 +110,7 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -109,6 +119,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for nm, v in zip(names, parts[5:9]):
@@ -117,37 +128,399 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "power_w_max": max(power), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def profile_traffic(kernel_tag: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel, or
-    None if there is none or the kernel's source changed since the capture."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+def profile_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None if there is none or the kernel's source changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    src = os.path.join(ROOT, "fp8_fine_grained_amax_gb300", "csrc", "gemm.cu")
-    if not m or not h:
+    f = re.search(r"source_file:\s*(\S+)", text)
+    if not m or not h or not f:
+        return None
+    src = os.path.join(CSRC, f.group(1))
+    if not os.path.exists(src):
         return None
     cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
     return float(m.group(1)) if cur == h.group(1) else None
 
 
+def _pinned(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16) \
+        .pin_memory()
+
+
 # ----------------------------------------------------------------- workloads
-def make_inputs(workload: str):
-    from fp8_fine_grained_amax_gb300 import synth
-    if workload == "fprop_4096x7168x7168":
-        M, N, K = 4096, 7168, 7168
-        return dict(M=M, N=N, K=K, X=synth.activation(M, K, seed=0, name="fprop.X"),
-                    W=synth.weight(N, K, seed=0, name="fprop.W"))
-    if workload.startswith("square_"):
-        n = int(workload.split("_")[1])
-        return dict(M=n, N=n, K=n, X=synth.activation(n, n, seed=0, name=f"square{n}.X"),
-                    W=synth.weight(n, n, seed=0, name=f"square{n}.W"))
-    raise SystemExit(f"unknown workload {workload}")
+class Kernel:
+    """One launch of the step: name, call, algorithmic work and its bound."""
+
+    def __init__(self, name, fn, work, bound):
+        self.name, self.fn, self.work, self.bound = name, fn, work, bound
+
+
+class Workload:
+    unit = "TFLOP/s"
+
+    def host_inputs(self):            # name -> BF16 bits / int arrays
+        raise NotImplementedError
+
+    def setup(self, dev, inp):         # device tensors; pinned host copies
+        raise NotImplementedError
+
+    def kernels(self, st, stream):     # list of Kernel
+        raise NotImplementedError
+
+    def h2d(self, st):                  # copy the step's inputs host -> device
+        for name, (host, dev) in st["io_in"].items():
+            dev.copy_(host, non_blocking=True)
+
+    def d2h(self, st):
+        for name, (host, dev) in st["io_out"].items():
+            host.copy_(dev, non_blocking=True)
+
+    def io_bytes(self, st):
+        bi = sum(h.numel() * h.element_size() for h, _ in st["io_in"].values())
+        bo = sum(h.numel() * h.element_size() for h, _ in st["io_out"].values())
+        return bi, bo
+
+    def work_per_step(self, st, stream):
+        return sum(k.work for k in self.kernels(st, stream) if k.bound == self.work_bound)
+
+    work_bound = "tensor"
+
+
+class Fprop(Workload):
+    def __init__(self, name, M, N, K):
+        self.name, self.M, self.N, self.K = name, M, N, K
+        self.config = {"M": M, "N": N, "K": K,
+                       "step": "quant_act(X) + quant_weight(W) + fp8_gemm -> bf16"}
+
+    def host_inputs(self):
+        from fp8_fine_grained_amax_gb300 import synth
+        tag = self.name
+        return {"X": synth.activation(self.M, self.K, seed=0, name=f"{tag}.X"),
+                "W": synth.weight(self.N, self.K, seed=0, name=f"{tag}.W")}
+
+    def setup(self, dev, inp):
+        import torch
+        M, N, K = self.M, self.N, self.K
+        st = {"X_h": _pinned(inp["X"]), "W_h": _pinned(inp["W"])}
+        st["X"], st["W"] = st["X_h"].to(dev), st["W_h"].to(dev)
+        st["qa"] = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        st["sa"] = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        st["qb"] = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        st["sb"] = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
+        st["C"] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        st["io_in"] = {"X": (st["X_h"], st["X"]), "W": (st["W_h"], st["W"])}
+        st["io_out"] = {"C": (torch.empty((M, N), dtype=torch.bfloat16).pin_memory(), st["C"])}
+        return st
+
+    def kernels(self, st, stream):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        M, N, K = self.M, self.N, self.K
+        return [
+            Kernel("quant_act_kernel",
+                   lambda: B.fp8q_quant_act(st["X"], q=st["qa"], sa=st["sa"], stream=stream),
+                   M * K * 2 + M * K + (K // 128) * M * 4, "hbm"),
+            Kernel("quant_weight_kernel",
+                   lambda: B.fp8q_quant_weight(st["W"], q=st["qb"], sb=st["sb"], stream=stream),
+                   N * K * 3 + ((N + 127) // 128) * (K // 128) * 4, "hbm"),
+            Kernel("fp8q_gemm_kernel",
+                   lambda: B.fp8q_gemm(st["qa"], st["sa"], st["qb"], st["sb"], c=st["C"],
+                                       stream=stream),
+                   2.0 * M * N * K, "tensor"),
+        ]
+
+    def cpu_step(self, inp, target_s):
+        import oracle
+        M, N, K = self.M, self.N, self.K
+        t0 = time.perf_counter()
+        qa, sa = oracle.quant_act(inp["X"])
+        t_act = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        qb, sb = oracle.quant_weight(inp["W"])
+        t_w = time.perf_counter() - t0
+        rows, t_g = _sampled_rows(
+            lambda r: oracle.gemm_rows(qa, sa, qb, sb, oracle.BSCALE_BLOCK, r), M,
+            target_s - t_act - t_w)
+        step_s = t_act + t_w + t_g * M / rows
+        return step_s, (f"quant_act {M}x{K} and quant_weight {N}x{K} in full "
+                        f"({t_act:.2f} s + {t_w:.2f} s); GEMM on {rows} of {M} rows "
+                        f"({t_g:.2f} s), extrapolated linearly to {M} rows"), t_act + t_w + t_g
+
+
+class LinearBwd(Workload):
+    """Backward of Y = X W^T with X [T][d_in], W [d_out][d_in], dY [T][d_out]."""
+
+    def __init__(self, T=8192, d_in=7168, d_out=2048):
+        self.name = f"linear_bwd_T{T}"
+        self.T, self.d_in, self.d_out = T, d_in, d_out
+        self.config = {"T": T, "d_in": d_in, "d_out": d_out,
+                       "step": "quant_act_T(dY, fused 1x128) + quant_act_T(X) + "
+                               "quant_weight(W, transposed) + Dgrad (bf16) + Wgrad (fp32)"}
+
+    def host_inputs(self):
+        from fp8_fine_grained_amax_gb300 import synth
+        T, di, do = self.T, self.d_in, self.d_out
+        return {"dY": synth.normal_bf16((T, do), 1e-3, 0, "bwd.dY"),
+                "X": synth.activation(T, di, seed=0, name="bwd.X"),
+                "W": synth.weight(do, di, seed=0, name="bwd.W")}
+
+    def setup(self, dev, inp):
+        import torch
+        T, di, do = self.T, self.d_in, self.d_out
+        u8, f32 = torch.uint8, torch.float32
+        st = {k + "_h": _pinned(v) for k, v in inp.items()}
+        for k in inp:
+            st[k] = st[k + "_h"].to(dev)
+        e = lambda *s, dt=u8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+        st.update(qdyT=e(do, T), sdyT=e(T // 128, do, dt=f32), qdy=e(T, do),
+                  sdy=e(do // 128, T, dt=f32), qxT=e(di, T), sxT=e(T // 128, di, dt=f32),
+                  qw=e(do, di), sw=e(do // 128, di // 128, dt=f32), qwT=e(di, do),
+                  dX=e(T, di, dt=torch.bfloat16), dW=e(do, di, dt=f32))
+        st["io_in"] = {k: (st[k + "_h"], st[k]) for k in inp}
+        st["io_out"] = {"dX": (torch.empty((T, di), dtype=torch.bfloat16).pin_memory(), st["dX"]),
+                        "dW": (torch.empty((do, di), dtype=f32).pin_memory(), st["dW"])}
+        return st
+
+    def kernels(self, st, stream):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        T, di, do = self.T, self.d_in, self.d_out
+        return [
+            Kernel("quant_act_T_kernel(dY,rows)", lambda: B.fp8q_quant_act_T(
+                st["dY"], with_rows=True, qT=st["qdyT"], sT=st["sdyT"], q_rows=st["qdy"],
+                s_rows=st["sdy"], stream=stream), T * do * 4 + (T // 128) * do * 4 +
+                (do // 128) * T * 4, "hbm"),
+            Kernel("quant_act_T_kernel(X)", lambda: B.fp8q_quant_act_T(
+                st["X"], qT=st["qxT"], sT=st["sxT"], stream=stream),
+                T * di * 3 + (T // 128) * di * 4, "hbm"),
+            Kernel("quant_weight_kernel(T)", lambda: B.fp8q_quant_weight(
+                st["W"], with_transpose=True, q=st["qw"], qT=st["qwT"], sb=st["sw"],
+                stream=stream), do * di * 4 + (do // 128) * (di // 128) * 4, "hbm"),
+            Kernel("fp8q_gemm_kernel(dgrad)", lambda: B.fp8q_gemm(
+                st["qdy"], st["sdy"], st["qwT"], st["sw"], bscale_kind=B.FP8Q_BSCALE_BLOCK_T,
+                c=st["dX"], stream=stream), 2.0 * T * di * do, "tensor"),
+            Kernel("fp8q_gemm_kernel(wgrad)", lambda: B.fp8q_gemm(
+                st["qdyT"], st["sdyT"], st["qxT"], st["sxT"], bscale_kind=B.FP8Q_BSCALE_ROW,
+                out_dtype=B.FP8Q_OUT_FP32, c=st["dW"], stream=stream), 2.0 * do * di * T,
+                "tensor"),
+        ]
+
+    def cpu_step(self, inp, target_s):
+        import oracle
+        T, di, do = self.T, self.d_in, self.d_out
+        t0 = time.perf_counter()
+        qdyT, sdyT = oracle.quant_act_T(inp["dY"])
+        qdy, sdy = oracle.quant_act(inp["dY"])
+        qxT, sxT = oracle.quant_act_T(inp["X"])
+        qw, sw = oracle.quant_weight(inp["W"])
+        qwT = np.ascontiguousarray(qw.T)
+        t_q = time.perf_counter() - t0
+        budget = (target_s - t_q) / 2
+        rd, t_d = _sampled_rows(lambda r: oracle.gemm_rows(qdy, sdy, qwT, sw,
+                                                           oracle.BSCALE_BLOCK_T, r), T, budget)
+        rw, t_w = _sampled_rows(lambda r: oracle.gemm_rows(qdyT, sdyT, qxT, sxT,
+                                                           oracle.BSCALE_ROW, r), do, budget)
+        step_s = t_q + t_d * T / rd + t_w * do / rw
+        return step_s, (f"all quantisers in full ({t_q:.2f} s); Dgrad on {rd} of {T} rows "
+                        f"({t_d:.2f} s) and Wgrad on {rw} of {do} rows ({t_w:.2f} s), "
+                        "extrapolated linearly"), t_q + t_d + t_w
+
+
+class MoEFprop(Workload):
+    def __init__(self, G=16, tokens=16384, d_model=7168, d_ff=4096, d_down_in=2048):
+        self.name = f"moe_fprop_{G}x{tokens}"
+        self.G, self.T, self.dm, self.dff, self.ddi = G, tokens, d_model, d_ff, d_down_in
+        self.config = {"experts": G, "tokens": tokens, "up": f"{d_model}->{d_ff}",
+                       "down": f"{d_down_in}->{d_model}", "routing": "Dirichlet(0.5) top-1",
+                       "step": "quant_act(X) + quant_weight(W_up, all experts) + grouped GEMM "
+                               "up; quant_act(H) + quant_weight(W_down) + grouped GEMM down"}
+
+    def host_inputs(self):
+        from fp8_fine_grained_amax_gb300 import synth
+        G, T = self.G, self.T
+        return {"offs": synth.moe_offsets(T, G, 0.5, seed=0),
+                "X": synth.activation(T, self.dm, seed=0, name="moe.X"),
+                "H": synth.normal_bf16((T, self.ddi), 1.0, 0, "moe.H"),
+                "Wup": synth.weight(G * self.dff, self.dm, seed=0, name="moe.Wup"),
+                "Wdown": synth.weight(G * self.dm, self.ddi, seed=0, name="moe.Wdown")}
+
+    def setup(self, dev, inp):
+        import torch
+        G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
+        u8, f32 = torch.uint8, torch.float32
+        st = {k + "_h": _pinned(inp[k]) for k in ("X", "H", "Wup", "Wdown")}
+        for k in ("X", "H", "Wup", "Wdown"):
+            st[k] = st[k + "_h"].to(dev)
+        st["offs"] = torch.from_numpy(inp["offs"]).to(dev)
+        e = lambda *s, dt=u8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+        st.update(qx=e(T, dm), sx=e(dm // 128, T, dt=f32), qh=e(T, ddi), sh=e(ddi // 128, T, dt=f32),
+                  qup=e(G * dff, dm), sup=e(G * dff // 128, dm // 128, dt=f32),
+                  qdn=e(G * dm, ddi), sdn=e(G * dm // 128, ddi // 128, dt=f32),
+                  Yup=e(T, dff, dt=torch.bfloat16), Ydn=e(T, dm, dt=torch.bfloat16))
+        st["io_in"] = {k: (st[k + "_h"], st[k]) for k in ("X", "H", "Wup", "Wdown")}
+        st["io_out"] = {"Yup": (torch.empty((T, dff), dtype=torch.bfloat16).pin_memory(),
+                                st["Yup"]),
+                        "Ydn": (torch.empty((T, dm), dtype=torch.bfloat16).pin_memory(),
+                                st["Ydn"])}
+        return st
+
+    def kernels(self, st, stream):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
+        return [
+            Kernel("quant_act_kernel(X)", lambda: B.fp8q_quant_act(
+                st["X"], q=st["qx"], sa=st["sx"], stream=stream), T * dm * 3 + T * dm // 32, "hbm"),
+            Kernel("quant_weight_kernel(Wup)", lambda: B.fp8q_quant_weight(
+                st["Wup"], q=st["qup"], sb=st["sup"], stream=stream), G * dff * dm * 3, "hbm"),
+            Kernel("fp8q_gemm_kernel(grouped up)", lambda: B.fp8q_grouped_gemm(
+                st["qx"], st["sx"], st["qup"].view(G, dff, dm),
+                st["sup"].view(G, dff // 128, dm // 128), st["offs"], c=st["Yup"],
+                stream=stream), 2.0 * T * dff * dm, "tensor"),
+            Kernel("quant_act_kernel(H)", lambda: B.fp8q_quant_act(
+                st["H"], q=st["qh"], sa=st["sh"], stream=stream), T * ddi * 3 + T * ddi // 32,
+                "hbm"),
+            Kernel("quant_weight_kernel(Wdown)", lambda: B.fp8q_quant_weight(
+                st["Wdown"], q=st["qdn"], sb=st["sdn"], stream=stream), G * dm * ddi * 3, "hbm"),
+            Kernel("fp8q_gemm_kernel(grouped down)", lambda: B.fp8q_grouped_gemm(
+                st["qh"], st["sh"], st["qdn"].view(G, dm, ddi),
+                st["sdn"].view(G, dm // 128, ddi // 128), st["offs"], c=st["Ydn"],
+                stream=stream), 2.0 * T * dm * ddi, "tensor"),
+        ]
+
+    def cpu_step(self, inp, target_s):
+        import oracle
+        G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
+        t0 = time.perf_counter()
+        qx, sx = oracle.quant_act(inp["X"])
+        qh, sh = oracle.quant_act(inp["H"])
+        qup, sup = oracle.quant_weight(inp["Wup"])
+        qdn, sdn = oracle.quant_weight(inp["Wdown"])
+        t_q = time.perf_counter() - t0
+        budget = (target_s - t_q) / 2
+        offs = inp["offs"]
+        ru, t_u = _sampled_rows(lambda r: oracle.grouped_gemm_rows(
+            qx, sx, qup.reshape(G, dff, dm), sup.reshape(G, dff // 128, dm // 128), offs, r),
+            T, budget)
+        rd, t_d = _sampled_rows(lambda r: oracle.grouped_gemm_rows(
+            qh, sh, qdn.reshape(G, dm, ddi), sdn.reshape(G, dm // 128, ddi // 128), offs, r),
+            T, budget)
+        step_s = t_q + t_u * T / ru + t_d * T / rd
+        return step_s, (f"all quantisers in full ({t_q:.2f} s); grouped GEMMs on {ru} and {rd} "
+                        f"of {T} rows ({t_u:.2f} s, {t_d:.2f} s), extrapolated linearly"), \
+            t_q + t_u + t_d
+
+
+class QuantOnly(Workload):
+    unit = "GB/s"
+    work_bound = "hbm"
+
+    def __init__(self, kind, rows, cols=7168):
+        self.kind, self.rows, self.cols = kind, rows, cols
+        self.name = f"{kind}_{rows}" if kind != "quant_weight" else f"quant_weight_{rows // 4096}x4096"
+        self.config = {"rows": rows, "cols": cols, "step": kind}
+
+    def host_inputs(self):
+        from fp8_fine_grained_amax_gb300 import synth
+        if self.kind == "quant_weight":
+            return {"X": synth.weight(self.rows, self.cols, seed=0, name=f"sweep.W{self.rows}")}
+        return {"X": synth.activation(self.rows, self.cols, seed=0, name=f"sweep.X{self.rows}")}
+
+    def setup(self, dev, inp):
+        import torch
+        R, C = self.rows, self.cols
+        st = {"X_h": _pinned(inp["X"])}
+        st["X"] = st["X_h"].to(dev)
+        if self.kind == "quant_act_T":
+            st["q"] = torch.empty((C, R), dtype=torch.uint8, device=dev)
+            st["s"] = torch.empty((R // 128, C), dtype=torch.float32, device=dev)
+        elif self.kind == "quant_weight":
+            st["q"] = torch.empty((R, C), dtype=torch.uint8, device=dev)
+            st["s"] = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
+        else:
+            st["q"] = torch.empty((R, C), dtype=torch.uint8, device=dev)
+            st["s"] = torch.empty((C // 128, R), dtype=torch.float32, device=dev)
+        st["io_in"] = {"X": (st["X_h"], st["X"])}
+        st["io_out"] = {"q": (torch.empty(st["q"].shape, dtype=torch.uint8).pin_memory(),
+                              st["q"])}
+        return st
+
+    def kernels(self, st, stream):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        R, C = self.rows, self.cols
+        if self.kind == "quant_act_T":
+            return [Kernel("quant_act_T_kernel", lambda: B.fp8q_quant_act_T(
+                st["X"], qT=st["q"], sT=st["s"], stream=stream), R * C * 3 + R * C // 32, "hbm")]
+        if self.kind == "quant_weight":
+            return [Kernel("quant_weight_kernel", lambda: B.fp8q_quant_weight(
+                st["X"], q=st["q"], sb=st["s"], stream=stream), R * C * 3, "hbm")]
+        mode = B.FP8Q_SCALE_POW2 if self.kind == "quant_act_pow2" else B.FP8Q_SCALE_FP32
+        return [Kernel("quant_act_kernel", lambda: B.fp8q_quant_act(
+            st["X"], q=st["q"], sa=st["s"], scale_mode=mode, stream=stream),
+            R * C * 3 + R * C // 32, "hbm")]
+
+    def cpu_step(self, inp, target_s):
+        import oracle
+        t0 = time.perf_counter()
+        if self.kind == "quant_act_T":
+            oracle.quant_act_T(inp["X"])
+        elif self.kind == "quant_weight":
+            oracle.quant_weight(inp["X"])
+        else:
+            oracle.quant_act(inp["X"], self.kind == "quant_act_pow2")
+        t = time.perf_counter() - t0
+        return t, f"{self.kind} on the full {self.rows}x{self.cols} input ({t:.2f} s)", t
+
+
+def _sampled_rows(run, M, budget_s):
+    """Time `run(rows)` on a seeded row sample sized to about budget_s seconds."""
+    rows = min(M, 8)
+    t0 = time.perf_counter()
+    run(np.arange(rows))
+    t_probe = time.perf_counter() - t0
+    n = int(min(M, max(rows, rows * max(budget_s, 0.5) / max(t_probe, 1e-3))))
+    sample = np.sort(np.random.default_rng(0).choice(M, size=n, replace=False))
+    t0 = time.perf_counter()
+    run(sample)
+    return n, time.perf_counter() - t0
+
+
+def make_workload(name: str) -> Workload:
+    if name == "fprop_4096x7168x7168":
+        return Fprop(name, 4096, 7168, 7168)
+    if name == "tiny_fprop":
+        return Fprop(name, 256, 256, 512)
+    if name.startswith("square_"):
+        n = int(name.split("_")[1])
+        return Fprop(name, n, n, n)
+    if name == "linear_bwd_T8192":
+        return LinearBwd()
+    if name == "moe_fprop_16x16384":
+        return MoEFprop()
+    for kind in ("quant_act_pow2", "quant_act_T", "quant_act"):
+        if name.startswith(kind + "_"):
+            return QuantOnly(kind, int(name[len(kind) + 1:]))
+    if name.startswith("quant_weight_") and name.endswith("x4096"):
+        return QuantOnly("quant_weight", int(name[len("quant_weight_"):-len("x4096")]) * 4096)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def cpu_baseline(wl: Workload, inp, target_s: float):
+    """The oracle, as it stands, on a bounded sample of one step; extrapolated
+    to the full step and reported in the metric's unit."""
+    import oracle
+    step_s, sample, spent = wl.cpu_step(inp, target_s)
+    work = wl.cpu_work
+    scale = 1e12 if wl.unit == "TFLOP/s" else 1e9
+    return {"value": round(work / step_s / scale, 6), "unit": wl.unit,
+            "cores": oracle.num_threads(), "kind": "oracle", "sample": sample,
+            "seconds": round(spent, 2)}
 
 
 # ----------------------------------------------------------------- our arm
@@ -168,35 +541,19 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     B.load_library()
 
-    inp = make_inputs(args.workload)
-    M, N, K = inp["M"], inp["N"], inp["K"]
-
-    def to_pinned(bits):
-        t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
-        return t.pin_memory()
-
-    X_h, W_h = to_pinned(inp["X"]), to_pinned(inp["W"])
-    X, W = X_h.to(dev), W_h.to(dev)
-    qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
-    qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
-    sb = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
-    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    C_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    wl = make_workload(args.workload)
+    inp = wl.host_inputs()
+    st = wl.setup(dev, inp)
     stream = torch.cuda.current_stream(dev)
+    ks = wl.kernels(st, stream)
 
     def step(ev=None):
+        for i, k in enumerate(ks):
+            if ev is not None:
+                ev[i].record(stream)
+            k.fn()
         if ev is not None:
-            ev[0].record(stream)
-        B.fp8q_quant_act(X, q=qa, sa=sa, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        B.fp8q_quant_weight(W, q=qb, sb=sb, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-        B.fp8q_gemm(qa, sa, qb, sb, c=C, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
+            ev[len(ks)].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -204,7 +561,8 @@ def run_ours(args, rank, world, local):
     if B.fp8q_sync_status(stream) != 0:
         raise SystemExit("device status error during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ks) + 1)]
+           for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -222,27 +580,23 @@ def run_ours(args, rank, world, local):
     status = B.fp8q_sync_status(stream)
     if status != 0:
         raise SystemExit(f"device status {status} after the timed region")
-    k_act = [e[0].elapsed_time(e[1]) for e in evs]
-    k_w = [e[1].elapsed_time(e[2]) for e in evs]
-    k_gemm = [e[2].elapsed_time(e[3]) for e in evs]
+    kms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(len(ks))]
 
-    # end to end through host buffers: H2D of X and W from pinned memory,
-    # the three kernels, D2H of C to pinned memory, every step
+    # end to end through host buffers: H2D of the step's inputs from pinned
+    # memory, the step's kernels, D2H of the step's results, every step
     e2e_steps = max(3, min(20, args.steps))
     for _ in range(2):
-        X.copy_(X_h, non_blocking=True)
-        W.copy_(W_h, non_blocking=True)
+        wl.h2d(st)
         step()
-        C_h.copy_(C, non_blocking=True)
+        wl.d2h(st)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        X.copy_(X_h, non_blocking=True)
-        W.copy_(W_h, non_blocking=True)
+        wl.h2d(st)
         step()
-        C_h.copy_(C, non_blocking=True)
+        wl.d2h(st)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -257,18 +611,42 @@ def run_ours(args, rank, world, local):
             dist.destroy_process_group()
         return None
 
-    flops = 2.0 * M * N * K
     hbm, bf16, bf16_sus, src = peaks()
     fp8_peak = bf16 * FP8_OVER_BF16
-    gemm_ms = statistics.mean(k_gemm)
-    act_ms, w_ms = statistics.mean(k_act), statistics.mean(k_w)
-    act_bytes = M * K * 2 + M * K + (K // 128) * M * 4
-    w_bytes = N * K * 2 + N * K + ((N + 127) // 128) * (K // 128) * 4
-    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    scale = 1e12 if wl.unit == "TFLOP/s" else 1e9
+    work = sum(k.work for k in ks if k.bound == wl.work_bound)
+    kernels = {}
+    for k, ms in zip(ks, kms):
+        if k.bound == "tensor":
+            a = k.work / (ms * 1e-3) / 1e12
+            kernels[k.name] = {"ms": round(ms, 5), "tflops": round(a, 1),
+                               "frac_fp8_peak": round(a / fp8_peak, 4)}
+        else:
+            a = k.work / (ms * 1e-3) / 1e9
+            kernels[k.name] = {"ms": round(ms, 5), "gbs": round(a, 1),
+                               "frac_hbm": round(a / hbm, 4)}
+    dom_i = max(range(len(ks)), key=lambda i: kms[i])
+    dom = ks[dom_i]
+    base_name = dom.name.split("(")[0]
+    if dom.bound == "tensor":
+        ach = dom.work / (kms[dom_i] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
+                "peak_source": f"{src}: bf16 burst {bf16} TFLOP/s x {FP8_OVER_BF16} "
+                               "(nominal fp8/bf16 ratio)"}
+    else:
+        ach = dom.work / (kms[dom_i] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "peak_source": f"{src}: HBM copy bandwidth"}
+    roof["traffic"] = profile_traffic(base_name, wl.name)
+    roof["kernel"] = dom.name
+    roof["work_per_launch"] = dom.work
+    in_bytes = sum(h.numel() * h.element_size() for h, _ in st["io_in"].values())
+    bi, bo = wl.io_bytes(st)
     line = {
         "metric": METRIC,
-        "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2),
-        "unit": "TFLOP/s",
+        "value": round(world * work / (ms_step * 1e-3) / scale, 2),
+        "unit": wl.unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -276,111 +654,77 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)",
+        "dtype": "fp8_e4m3 (fp32 accumulate)" if wl.unit == "TFLOP/s" else "bf16 -> e4m3",
         "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "N": N, "K": K,
-                   "step": "quant_act(X) + quant_weight(W) + fp8_gemm -> bf16",
-                   "l2": f"inputs larger than L2 ({(M * K + N * K) * 2 / 1e6:.0f} MB BF16 "
-                         f"read per step > {L2_BYTES / 1e6:.0f} MB); no flush",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
-                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / fp8_peak, 4),
-                     "traffic": profile_traffic(f"gemm_fprop_{M}x{N}x{K}"),
-                     "kernel": "fp8q_gemm_kernel",
-                     "peak_source": f"{src}: bf16 burst {bf16} TFLOP/s x {FP8_OVER_BF16} "
-                                    "(nominal fp8/bf16 ratio)"},
-        "kernels": {
-            "fp8q_gemm_kernel": {"ms": round(gemm_ms, 5), "tflops": round(gemm_tflops, 1),
-                                 "frac_fp8_peak": round(gemm_tflops / fp8_peak, 4)},
-            "quant_act_kernel": {"ms": round(act_ms, 5),
-                                 "gbs": round(act_bytes / (act_ms * 1e-3) / 1e9, 1),
-                                 "frac_hbm": round(act_bytes / (act_ms * 1e-3) / 1e9 / hbm, 4)},
-            "quant_weight_kernel": {"ms": round(w_ms, 5),
-                                    "gbs": round(w_bytes / (w_ms * 1e-3) / 1e9, 1),
-                                    "frac_hbm": round(w_bytes / (w_ms * 1e-3) / 1e9 / hbm, 4)},
-            "hbm_peak_gbs": hbm, "peak_source": src},
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": (M * K + N * K) * 2, "d2h_bytes_per_step": M * N * 2,
+        "config": dict(workload=wl.name, **wl.config,
+                       l2=f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step > "
+                          f"{L2_BYTES / 1e6:.0f} MB); no flush" if in_bytes > L2_BYTES else
+                          f"inputs {in_bytes / 1e6:.0f} MB fit in L2; no flush",
+                       parallelism=f"replicas x{world}"),
+        "roofline": roof,
+        "kernels": dict(kernels, hbm_peak_gbs=hbm, fp8_peak_tflops=round(fp8_peak, 1),
+                        peak_source=src),
+        "e2e": {"value": round(world * work / (e2e_ms * 1e-3) / scale, 2), "unit": wl.unit,
+                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": len(ks) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        wl.cpu_work = work
+        line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
     if world > 1:
         dist.destroy_process_group()
     return line
 
 
-# ----------------------------------------------------------------- CPU oracle
-def cpu_baseline(inp, target_s: float):
-    """The oracle, as it stands, on a bounded sample of the step; extrapolated
-    to the full step and reported in the metric's unit (TFLOP/s)."""
-    import oracle
-    M, N, K = inp["M"], inp["N"], inp["K"]
-    X, W = inp["X"], inp["W"]
-    qa, sa = oracle.quant_act(X)           # full quantisers (fast enough), timed below
-    qb, sb = oracle.quant_weight(W)
-    t0 = time.perf_counter()
-    qa, sa = oracle.quant_act(X)
-    t_act = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    qb, sb = oracle.quant_weight(W)
-    t_w = time.perf_counter() - t0
-    rows = 8
-    t0 = time.perf_counter()
-    oracle.gemm_rows(qa, sa, qb, sb, oracle.BSCALE_BLOCK, np.arange(rows))
-    t_probe = time.perf_counter() - t0
-    budget = max(1.0, target_s - t_act - t_w - t_probe)
-    rows = int(min(M, max(8, rows * budget / max(t_probe, 1e-3))))
-    rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(M, size=rows, replace=False))
-    t0 = time.perf_counter()
-    oracle.gemm_rows(qa, sa, qb, sb, oracle.BSCALE_BLOCK, sample)
-    t_gemm = time.perf_counter() - t0
-    step_s = t_act + t_w + t_gemm * (M / rows)
-    return {"value": round(2.0 * M * N * K / step_s / 1e12, 6), "unit": "TFLOP/s",
-            "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"quant_act {M}x{K} and quant_weight {N}x{K} in full "
-                      f"({t_act:.2f} s + {t_w:.2f} s); GEMM on {rows} of {M} rows "
-                      f"({t_gemm:.2f} s), extrapolated linearly to {M} rows",
-            "seconds": round(t_act + t_w + t_gemm, 2)}
-
-
+# ----------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """Reference arm: the CPU oracle on the host cores, same metric and config."""
     if rank != 0:
         return None
-    inp = make_inputs(args.workload)
-    M, N, K = inp["M"], inp["N"], inp["K"]
+    wl = make_workload(args.workload)
+    inp = wl.host_inputs()
+    wl.cpu_work = _work_of(wl)
     per_step = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     vals = []
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(inp, per_step)
+        cb = cpu_baseline(wl, inp, per_step)
         if i >= args.warmup:
             vals.append(cb)
     value = statistics.median(v["value"] for v in vals)
-    step_ms = 2.0 * M * N * K / (value * 1e12) * 1e3
+    scale = 1e12 if wl.unit == "TFLOP/s" else 1e9
     cb = dict(vals[-1])
     cb["value"] = value
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": wl.unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "N": N, "K": K,
-                   "step": "quant_act(X) + quant_weight(W) + scaled GEMM (CPU oracle)"},
+        "ms_per_step": round(wl.cpu_work / (value * scale) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": dict(workload=wl.name, **wl.config, implementation="CPU oracle"),
         "cpu_baseline": cb,
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+def _work_of(wl: Workload) -> float:
+    """Algorithmic work of one step without a GPU (same formulas as kernels())."""
+    if isinstance(wl, Fprop):
+        return 2.0 * wl.M * wl.N * wl.K
+    if isinstance(wl, LinearBwd):
+        return 2 * 2.0 * wl.T * wl.d_in * wl.d_out
+    if isinstance(wl, MoEFprop):
+        return 2.0 * wl.T * wl.dff * wl.dm + 2.0 * wl.T * wl.dm * wl.ddi
+    R, C = wl.rows, wl.cols
+    return R * C * 3 + (0 if wl.kind == "quant_weight" else R * C // 32)
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="fprop_4096x7168x7168")
