@@ -82,6 +82,8 @@ def _load():
                                                    I64, I64, P, I64, P, P]
             L.oracle_bf16_gemm_rows.restype = None
             L.oracle_bf16_gemm_rows.argtypes = [P, I64, P, I64, I64, I64, P, I64, P]
+            L.oracle_requant_act_T.restype = None
+            L.oracle_requant_act_T.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, INT]
             L.oracle_num_threads.restype = INT
             L.oracle_num_threads.argtypes = []
             _lib = L
@@ -159,6 +161,22 @@ def quant_weight(w_bf16: np.ndarray, pow2: bool = False):
     sb = np.empty(((N + 127) // 128, K // 128), np.float32)
     _load().oracle_quant_weight(_ptr(w), N, K, K, _ptr(q), K, _ptr(sb), int(bool(pow2)))
     return q, sb
+
+
+def requant_act_T(q, s_rows, pow2: bool = False):
+    """128x1 requantisation of FP8-cached 1x128 activations.
+
+    q [T][C] E4M3 codes with 1x128 scales s_rows [C/128][T] -> qT [C][T],
+    sT [T/128][C] (each value dequantised by one FP32 multiply first)."""
+    q = np.ascontiguousarray(q, np.uint8)
+    s_rows = np.ascontiguousarray(s_rows, np.float32)
+    T, C = q.shape
+    assert T % 128 == 0 and C % 128 == 0 and s_rows.shape == (C // 128, T)
+    qT = np.empty((C, T), np.uint8)
+    sT = np.empty((T // 128, C), np.float32)
+    _load().oracle_requant_act_T(_ptr(q), T, C, C, _ptr(s_rows), T, _ptr(qT), T, _ptr(sT), C,
+                                 int(bool(pow2)))
+    return qT, sT
 
 
 # ---------------------------------------------------------------- GEMMs

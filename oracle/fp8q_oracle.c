@@ -486,3 +486,61 @@ void oracle_bf16_gemm_rows(const uint16_t *x, int64_t ldx, const uint16_t *w,
   bgemm_ctx p = {x, w, ldx, ldw, N, K, rows, c};
   par_for(nrows * N, bgemm_item, &p);
 }
+
+/* ------------------------------------------------------------------------
+ * 128x1 requantisation from FP8-cached activations.  The forward pass keeps
+ * its activations in FP8 ([dssusan] paragraph 2, compressing cached
+ * activations; "Deepseek - Not For everyone" paragraph 3, caching activations
+ * in FP8 for the Linear's backward pass) as 1x128 tiles, and the backward
+ * pass needs the same tensor as 128x1 tiles ([dssusan] paragraph 4).
+ * READING: dequantise each cached value with one FP32 multiply rounded to
+ * nearest, x = fl32(decode(q) * s_row), then apply the 128x1 rule above to
+ * those FP32 values.
+ * q: E4M3 [T][C] (row stride ldq), s_rows: 1x128 scales s_rows[g * ld_s + t].
+ * qT: E4M3 [C][T] (row stride ldqT), sT[tg * ld_sT + c].  T % 128 == 0,
+ * C % 128 == 0.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const uint8_t *q;
+  const float *s_rows;
+  int64_t T, C, ldq, ld_s, ldqT, ld_sT;
+  uint8_t *qT;
+  float *sT;
+  int pow2;
+  double lut[256];
+} rq_ctx;
+
+static float dequant_f32(const rq_ctx *p, int64_t t, int64_t c) {
+  float v = (float)p->lut[p->q[t * p->ldq + c]];
+  return v * p->s_rows[(c / 128) * p->ld_s + t]; /* one FP32 multiply */
+}
+
+static void requant_T_channel(int64_t c, void *cx) {
+  rq_ctx *p = (rq_ctx *)cx;
+  for (int64_t tg = 0; tg < p->T / 128; ++tg) {
+    float amax = 0.0f;
+    for (int j = 0; j < 128; ++j) {
+      float v = fabsf(dequant_f32(p, tg * 128 + j, c));
+      if (v > amax) amax = v;
+    }
+    float s, inv;
+    oracle_group_scale(amax, p->pow2, &s, &inv);
+    p->sT[tg * p->ld_sT + c] = s;
+    for (int j = 0; j < 128; ++j) {
+      int64_t t = tg * 128 + j;
+      float prod = dequant_f32(p, t, c) * inv;
+      p->qT[c * p->ldqT + t] = oracle_e4m3_encode(prod);
+    }
+  }
+}
+
+void oracle_requant_act_T(const uint8_t *q, int64_t T, int64_t C, int64_t ldq,
+                          const float *s_rows, int64_t ld_s, uint8_t *qT,
+                          int64_t ldqT, float *sT, int64_t ld_sT, int pow2) {
+  rq_ctx *p = (rq_ctx *)malloc(sizeof(rq_ctx));
+  if (!p) return;
+  *p = (rq_ctx){q, s_rows, T, C, ldq, ld_s, ldqT, ld_sT, qT, sT, pow2, {0}};
+  for (int v = 0; v < 256; ++v) p->lut[v] = oracle_e4m3_decode((uint8_t)v);
+  par_for(C, requant_T_channel, p);
+  free(p);
+}

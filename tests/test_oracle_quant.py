@@ -189,3 +189,35 @@ def test_fp32_scale_is_single_division(oracle):
         s, inv = oracle.group_scale(amax, False)
         a = np.float32(amax)
         assert s == a / np.float32(448.0) and inv == np.float32(448.0) / a
+
+
+def test_requant_T_pow2_equals_quant_T_of_dequantised(oracle):
+    # with power-of-two 1x128 scales the dequantised values decode(q) * 2^e are
+    # exact and have at most 4 significant bits, so they are exact BF16 values:
+    # requantising the FP8 cache must then equal quantising those values 128x1
+    x = synth.activation(256, 384, seed=12)
+    q, s = oracle.quant_act(x, pow2=True)
+    deq = oracle.e4m3_decode(q) * np.repeat(s.T.astype(np.float64), 128, axis=1)
+    deq32 = deq.astype(np.float32)
+    assert np.array_equal(deq32.astype(np.float64), deq)
+    bits = f32_to_bf16_bits(deq32)
+    for pow2 in (False, True):
+        qT_ref, sT_ref = oracle.quant_act_T(bits, pow2)
+        qT, sT = oracle.requant_act_T(q, s, pow2)
+        assert np.array_equal(qT, qT_ref) and np.array_equal(sT, sT_ref)
+
+
+def test_requant_T_fp32_scales_invariants(oracle):
+    # FP32 1x128 scales: every channel group's max-abs dequantised value must
+    # land on +-448 again, and the codes stay within one E4M3 step of the
+    # values requantised in double precision
+    x = synth.activation(128, 256, seed=13)
+    q, s = oracle.quant_act(x)
+    qT, sT = oracle.requant_act_T(q, s)
+    deq = (oracle.e4m3_decode(q).astype(np.float32) * np.repeat(s.T, 128, axis=1)).astype(np.float32)
+    for c in range(256):
+        col = deq[:, c].astype(np.float64)
+        i = int(np.argmax(np.abs(col)))
+        if col[i] != 0:
+            assert oracle.e4m3_decode(qT[c, i]) == np.copysign(448.0, col[i])
+        assert sT[0, c] == np.float32(np.max(np.abs(deq[:, c]))) / np.float32(448.0)
