@@ -15,6 +15,8 @@ Other workloads (--workload):
   quant_act_pow2_<t>     same with power-of-two scales (GB/s)
   quant_act_T_<t>        128x1 transposed quantisation of t x 7168 (GB/s)
   quant_weight_<g>x4096  128x128 quantisation of g stacked 4096x7168 weights (GB/s)
+  quant_tensor_<t>       per-tensor quantisation of t x 7168, for comparison (GB/s)
+  linear_bwd_cached_T8192  the backward with X requantised from the FP8 cache
 
 Prints ONE JSON line (rank 0).  `value` is the step's algorithmic work (GEMM
 FLOPs 2MNK over real rows, or quantiser bytes) summed over ranks per second of
@@ -447,6 +449,53 @@ class MoEFprop(Workload):
             t_q + t_u + t_d
 
 
+class LinearBwdCached(LinearBwd):
+    """The same backward, with X taken from the forward pass's FP8 cache (1x128
+    codes and scales) and requantised 128x1 instead of read again as BF16."""
+
+    def __init__(self, T=8192, d_in=7168, d_out=2048):
+        super().__init__(T, d_in, d_out)
+        self.name = f"linear_bwd_cached_T{T}"
+        self.config = dict(self.config, step="quant_act_T(dY, fused 1x128) + requant_act_T(X "
+                           "from FP8 cache) + quant_weight(W, transposed) + Dgrad + Wgrad")
+
+    def setup(self, dev, inp, host=None):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        st = super().setup(dev, inp, host)
+        st["qx_cache"], st["sx_cache"] = B.fp8q_quant_act(st["X"])   # the forward pass's cache
+        return st
+
+    def kernels(self, st, stream):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        ks = super().kernels(st, stream)
+        T, di = self.T, self.d_in
+        ks[1] = Kernel("requant_act_T_kernel(X)", lambda: B.fp8q_requant_act_T(
+            st["qx_cache"], st["sx_cache"], qT=st["qxT"], sT=st["sxT"], stream=stream),
+            T * di * 2 + (di // 128) * T * 4 + (T // 128) * di * 4, "hbm")
+        return ks
+
+    def cpu_step(self, inp, target_s):
+        import oracle
+        T, di, do = self.T, self.d_in, self.d_out
+        qx, sx = oracle.quant_act(inp["X"])          # the forward pass's cache (not timed)
+        t0 = time.perf_counter()
+        qdyT, sdyT = oracle.quant_act_T(inp["dY"])
+        qdy, sdy = oracle.quant_act(inp["dY"])
+        qxT, sxT = oracle.requant_act_T(qx, sx)
+        qw, sw = oracle.quant_weight(inp["W"])
+        qwT = np.ascontiguousarray(qw.T)
+        t_q = time.perf_counter() - t0
+        budget = (target_s - t_q) / 2
+        rd, t_d = _sampled_rows(lambda r: oracle.gemm_rows(qdy, sdy, qwT, sw,
+                                                           oracle.BSCALE_BLOCK_T, r), T, budget)
+        rw, t_w = _sampled_rows(lambda r: oracle.gemm_rows(qdyT, sdyT, qxT, sxT,
+                                                           oracle.BSCALE_ROW, r), do, budget)
+        step_s = t_q + t_d * T / rd + t_w * do / rw
+        return step_s, (f"all quantisers in full ({t_q:.2f} s); Dgrad on {rd} of {T} rows "
+                        f"({t_d:.2f} s) and Wgrad on {rw} of {do} rows ({t_w:.2f} s), "
+                        "extrapolated linearly"), t_q + t_d + t_w
+
+
 class QuantOnly(Workload):
     unit = "GB/s"
     work_bound = "hbm"
@@ -489,6 +538,15 @@ class QuantOnly(Workload):
         if self.kind == "quant_weight":
             return [Kernel("quant_weight_kernel", lambda: B.fp8q_quant_weight(
                 st["X"], q=st["q"], sb=st["s"], stream=stream), R * C * 3, "hbm")]
+        if self.kind == "quant_tensor":
+            if "ws" not in st:
+                import torch
+                st["ws"] = torch.empty((B.fp8q_quant_tensor_workspace_bytes(R, C),),
+                                       dtype=torch.uint8, device=st["X"].device)
+                st["s1"] = torch.empty((1,), dtype=torch.float32, device=st["X"].device)
+            return [Kernel("tensor_amax+quant_kernels", lambda: B.fp8q_quant_tensor(
+                st["X"], q=st["q"], s=st["s1"], workspace=st["ws"], stream=stream),
+                R * C * 3, "hbm")]
         mode = B.FP8Q_SCALE_POW2 if self.kind == "quant_act_pow2" else B.FP8Q_SCALE_FP32
         return [Kernel("quant_act_kernel", lambda: B.fp8q_quant_act(
             st["X"], q=st["q"], sa=st["s"], scale_mode=mode, stream=stream),
@@ -499,6 +557,8 @@ class QuantOnly(Workload):
         t0 = time.perf_counter()
         if self.kind == "quant_act_T":
             oracle.quant_act_T(inp["X"])
+        elif self.kind == "quant_tensor":
+            oracle.quant_tensor(inp["X"])
         elif self.kind == "quant_weight":
             oracle.quant_weight(inp["X"])
         else:
@@ -532,7 +592,9 @@ def make_workload(name: str) -> Workload:
         return LinearBwd()
     if name == "moe_fprop_16x16384":
         return MoEFprop()
-    for kind in ("quant_act_pow2", "quant_act_T", "quant_act"):
+    if name == "linear_bwd_cached_T8192":
+        return LinearBwdCached()
+    for kind in ("quant_act_pow2", "quant_act_T", "quant_tensor", "quant_act"):
         if name.startswith(kind + "_"):
             return QuantOnly(kind, int(name[len(kind) + 1:]))
     if name.startswith("quant_weight_") and name.endswith("x4096"):
@@ -773,7 +835,7 @@ def _work_of(wl: Workload) -> float:
     if isinstance(wl, MoEFprop):
         return 2.0 * wl.T * wl.dff * wl.dm + 2.0 * wl.T * wl.dm * wl.ddi
     R, C = wl.rows, wl.cols
-    return R * C * 3 + (0 if wl.kind == "quant_weight" else R * C // 32)
+    return R * C * 3 + (0 if wl.kind in ("quant_weight", "quant_tensor") else R * C // 32)
 
 
 def main():

@@ -40,8 +40,13 @@ SIGNATURES = {
     "fp8q_quant_act_T": (_INT, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64,
                                 _INT, _P]),
     "fp8q_quant_weight": (_INT, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P]),
+    "fp8q_requant_act_T": (_INT, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P]),
+    "fp8q_quant_tensor_workspace_bytes": (_I64, [_I64, _I64]),
+    "fp8q_quant_tensor": (_INT, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _I64, _INT, _P]),
     "fp8q_gemm": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P, _I64, _INT, _I64,
                          _I64, _I64, _P]),
+    "fp8q_gemm_accumulate": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P, _I64, _I64,
+                                    _I64, _I64, _P]),
     "fp8q_grouped_gemm": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _INT, _P, _I64, _INT,
                                  _I64, _I64, _I64, _P]),
     "fp8q_cast_e4m3": (_INT, [_P, _I64, _P, _P]),
@@ -146,6 +151,22 @@ def fp8q_quant_act_T(x, *, scale_mode=FP8Q_SCALE_FP32, with_rows=False, qT=None,
     return qT, sT
 
 
+def fp8q_requant_act_T(q, s_rows, *, scale_mode=FP8Q_SCALE_FP32, qT=None, sT=None, stream=None):
+    """128x1 requantisation of FP8-cached 1x128 codes q uint8 [T][C] with scales
+    s_rows f32 [C/128][T] -> (qT uint8 [C][T], sT f32 [T/128][C])."""
+    T, C = q.shape
+    if qT is None:
+        qT = torch.empty((C, T), dtype=torch.uint8, device=q.device)
+    if sT is None:
+        sT = torch.empty((T // 128, C), dtype=torch.float32, device=q.device)
+    _check(load_library().fp8q_requant_act_T(
+        _ptr(q), T, C, _rows_ld(q, "q"), _ptr(s_rows),
+        _rows_ld(s_rows, "s_rows") if s_rows.numel() else T, _ptr(qT),
+        _rows_ld(qT, "qT") if qT.numel() else T, _ptr(sT), _rows_ld(sT, "sT") if sT.numel() else C,
+        scale_mode, _stream(stream)), "fp8q_requant_act_T")
+    return qT, sT
+
+
 def fp8q_quant_weight(w, *, scale_mode=FP8Q_SCALE_FP32, with_transpose=False, q=None, qT=None,
                       sb=None, stream=None):
     """128x128 quantisation of BF16 w [N][K] -> (q uint8 [N][K], sb f32 [ceil(N/128)][K/128]),
@@ -169,6 +190,30 @@ def fp8q_quant_weight(w, *, scale_mode=FP8Q_SCALE_FP32, with_transpose=False, q=
     return q, sb
 
 
+def fp8q_quant_tensor_workspace_bytes(M: int, K: int) -> int:
+    return int(load_library().fp8q_quant_tensor_workspace_bytes(M, K))
+
+
+def fp8q_quant_tensor(x, *, scale_mode=FP8Q_SCALE_FP32, q=None, s=None, workspace=None,
+                      stream=None):
+    """Per-tensor quantisation (comparison path): x BF16 [M][K] -> (q uint8 [M][K],
+    s f32 [1]).  A workspace tensor is allocated with torch when not given."""
+    M, K = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    if s is None:
+        s = torch.empty((1,), dtype=torch.float32, device=dev)
+    nbytes = fp8q_quant_tensor_workspace_bytes(M, K)
+    if workspace is None:
+        workspace = torch.empty((max(nbytes, 4),), dtype=torch.uint8, device=dev)
+    _check(load_library().fp8q_quant_tensor(
+        _ptr(x), M, K, _rows_ld(x, "x"), _ptr(q), _rows_ld(q, "q"), _ptr(s), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), scale_mode, _stream(stream)),
+        "fp8q_quant_tensor")
+    return q, s
+
+
 def fp8q_gemm(a, sa, b, sb, *, bscale_kind=FP8Q_BSCALE_BLOCK, out_dtype=FP8Q_OUT_BF16, c=None,
               stream=None):
     """C [M][N] = per-128-K-group scaled a [M][K] x b [N][K]^T (E4M3 codes)."""
@@ -183,6 +228,21 @@ def fp8q_gemm(a, sa, b, sb, *, bscale_kind=FP8Q_BSCALE_BLOCK, out_dtype=FP8Q_OUT
         _ptr(a), _rows_ld(a, "a") if a.numel() else K, _ptr(sa), ld_sa, _ptr(b),
         _rows_ld(b, "b") if b.numel() else K, _ptr(sb), ld_sb, bscale_kind, _ptr(c),
         _rows_ld(c, "c"), out_dtype, M, N, K, _stream(stream)), "fp8q_gemm")
+    return c
+
+
+def fp8q_gemm_accumulate(a, sa, b, sb, c, *, bscale_kind=FP8Q_BSCALE_BLOCK, stream=None):
+    """c (FP32 [M][N]) += per-128-K-group scaled a [M][K] x b [N][K]^T."""
+    M, K = a.shape
+    N = b.shape[0]
+    if c.dtype != torch.float32 or tuple(c.shape) != (M, N):
+        raise ValueError("c must be an FP32 [M][N] tensor")
+    ld_sa = _rows_ld(sa, "sa") if sa.numel() else M
+    ld_sb = _rows_ld(sb, "sb") if sb.numel() else 1
+    _check(load_library().fp8q_gemm_accumulate(
+        _ptr(a), _rows_ld(a, "a") if a.numel() else K, _ptr(sa), ld_sa, _ptr(b),
+        _rows_ld(b, "b") if b.numel() else K, _ptr(sb), ld_sb, bscale_kind, _ptr(c),
+        _rows_ld(c, "c"), M, N, K, _stream(stream)), "fp8q_gemm_accumulate")
     return c
 
 

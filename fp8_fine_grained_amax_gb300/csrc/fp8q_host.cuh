@@ -2,8 +2,10 @@
 // checks, argument validation and launch error mapping.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -50,5 +52,51 @@ inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3
 inline fp8q_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
+
+// Time limit of every device-side wait (fp8q_set_wait_timeout_ns).
+inline std::atomic<uint64_t> &wait_timeout_ns() {
+  static std::atomic<uint64_t> ns{2000000000ull};
+  return ns;
+}
+
+// The driver's tensor-map encoder, looked up through the runtime (no libcuda
+// link dependency).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D tensor [rows][cols] of `type` (elem_bytes each) with row pitch ld_bytes,
+// box box_cols x box_rows, zero fill outside the tensor.
+inline bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *base,
+                         uint64_t rows, uint64_t cols, uint64_t ld_bytes, uint32_t box_cols,
+                         uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Read (and clear) the quantisers' device status word; defined in quant.cu.
+fp8q_status quant_status_take(cudaStream_t s);
 
 }  // namespace fp8q

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 namespace fp8q {
@@ -53,17 +54,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, with acquire semantics at cluster scope: for barriers that receive
+// arrivals from the other CTA of a pair.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait.  Returns true when the phase completed; false when the CTA's
 // abort flag is raised or `limit_ns` has passed (then it raises the abort
 // flag itself and records `code` in the device status word).
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort_flag,
                                                   int *status_word, uint64_t limit_ns,
                                                   int code) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_wait = [&]() {
+    return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (try_wait()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait()) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
@@ -239,13 +258,33 @@ __device__ __forceinline__ void group_scale(float amax, bool pow2, float &s, flo
     return;
   }
   // a = 1.m * 2^E; 448 = 1.75 * 2^8.  For 1.m <= 1.75, e = E - 8; else E - 7.
+  // e is clamped to 127 (an infinite max-abs, reachable only when a value
+  // overflowed FP32 before quantisation, also gives 127); the floor on a
+  // keeps e >= -124, so s is always a normal FP32.  inv = 2^-e is normal for
+  // e <= 126 and the subnormal 2^-127 for e = 127.
   const uint32_t bits = __float_as_uint(a);
   const int E = static_cast<int>((bits >> 23) & 0xFF) - 127;
   const uint32_t mant = bits & 0x7FFFFF;
   int e = E - 8 + (mant > 0x600000u ? 1 : 0);
+  if (E > 127) e = 127;
   e = max(-126, min(127, e));
   s = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-  inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  inv = e <= 126 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23)
+                 : __uint_as_float(0x00400000u);
+}
+
+// Two E4M3 codes (low byte first) -> two FP16 values (exact: every E4M3 value
+// is an FP16 value), packed low half first.
+__device__ __forceinline__ uint32_t decode_e4m3x2(uint16_t codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes),
+                                                   __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFF)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -254,6 +293,84 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // max of |lo|, |hi| of a packed BF16 pair, as FP32 (exact).
 __device__ __forceinline__ float absmax_bf16x2(uint32_t w) {
   return fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w)));
+}
+
+}  // namespace fp8q
+
+namespace fp8q {
+
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs running tcgen05 with .cta_group::2: one MMA (M=256)
+// uses both CTAs' shared memory and writes both CTAs' tensor memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// All threads of all CTAs of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (may be the peer's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// TMEM allocation for a CTA pair (issued by one warp in each CTA of the pair).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t smem_slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D[tmem of both CTAs] (+)= A[smem of both CTAs] * B[smem of both CTAs]^T,
+// M = 256 (128 rows per CTA), issued by one thread of the pair.
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (count 1) on the mbarrier at the same offset in every CTA of
+// `cta_mask` once all tcgen05 operations issued so far by this thread are done.
+__device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// 2-D tiled TMA load into this CTA's shared memory whose completion is
+// signalled on an mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void *tmap,
+                                                 uint32_t bar_cluster_addr, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar_cluster_addr)
+      : "memory");
 }
 
 }  // namespace fp8q

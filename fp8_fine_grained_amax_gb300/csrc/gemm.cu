@@ -40,7 +40,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -56,8 +55,7 @@ __device__ int g_status;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int kStages = 4;
+constexpr int BM = 128, BN = 256, BK = 128;   // per-CTA rows, tile columns, K-group
 constexpr int kEpiWarps = 8;                     // 2 warpgroups: 4 TMEM lane quarters x 2
 constexpr int kEpiCols = BN / (kEpiWarps / 4);   // columns folded by each epilogue thread
 constexpr int kThreads = 128 + kEpiWarps * 32;   // control warpgroup + epilogue warpgroups
@@ -71,12 +69,33 @@ static_assert(kCtlRegs + (kWarpsPerSubpartition - 1) * kEpiRegs <=
               "register split must fit the launch allocation");
 static_assert(kLaunchRegs * kThreads <= 65536, "launch register budget");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kABytes = BM * BK;
-constexpr uint32_t kBBytes = BN * BK;
-constexpr uint32_t kIdesc = idesc_e4m3_f32(BM, BN);
 constexpr int kGroupM = 16;   // L2 rasterisation band (m-tiles) for the dense GEMM
 constexpr int kMaxGroups = 1024;
 constexpr uint64_t kDrainNs = 1000000000ull;  // 1 s for draining after an abort
+constexpr int kMaxStages = 6;
+constexpr bool kGroupedPair = false;  // tile shape of the grouped (MoE) GEMM
+constexpr bool kDensePair = false;    // tile shape of the dense GEMMs
+
+// Two shapes of the same pipeline:
+//  single CTA: tile 128 x 256 per CTA; ring stage = A 128 rows + B 256 rows.
+//  CTA pair  : tile 256 x 256 per cluster of two CTAs; each CTA stages its own
+//              128 rows of A and 128 rows (half the columns) of B, and one
+//              tcgen05.mma.cta_group::2 (M = 256) in the leading CTA reads both
+//              CTAs' shared memory and writes both CTAs' tensor memory.  Per SM
+//              that is 32 KB of operands per K-group instead of 48 KB, so six
+//              stages fit and each stage is refilled with a third less traffic.
+template <bool kPair>
+struct Cfg {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr uint32_t kABytes = BM * BK;                    // per CTA
+  static constexpr uint32_t kBBytes = (kPair ? BN / 2 : BN) * BK;  // per CTA
+  static constexpr int kTileM = kPair ? 2 * BM : BM;              // C rows per tile
+  static constexpr uint32_t kIdesc = idesc_e4m3_f32(kPair ? 2 * BM : BM, BN);
+  static constexpr uint32_t kTxBytes = (kPair ? 2 : 1) * (kABytes + kBBytes);
+  static constexpr int kTemptyCount = (kPair ? 2 : 1) * kEpiWarps;
+  static constexpr size_t kTileBytes = static_cast<size_t>(kStages) * (kABytes + kBBytes);
+  static_assert(kStages <= kMaxStages, "ring too deep for SmemCtl");
+};
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -88,6 +107,13 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > kDrainNs) return;
+}
+
+// Spin for `ns` nanoseconds (lets copies issued just before an abort land).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
 }
 
 struct GemmArgs {
@@ -105,28 +131,27 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-// Shared-memory layout (dynamic; tiles 1024-byte aligned for the swizzle).
+// Shared-memory control block, after the operand ring (1024-byte aligned).
 struct alignas(8) SmemCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
-  uint64_t sbfull[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  float sb_row[2][BN];
+  // per-column B scales (Wgrad): each epilogue warp stages the scales of its
+  // own columns for the current K-group, double-buffered
+  alignas(16) float sb_warp[kEpiWarps][2][kEpiCols];
 };
 
-constexpr size_t kTileBytes = static_cast<size_t>(kStages) * (kABytes + kBBytes);
-
-__host__ __device__ constexpr size_t smem_bytes(bool grouped) {
-  return 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl) +
-         (grouped ? 3 * (kMaxGroups + 1) * sizeof(int) : 0);
+__host__ __device__ constexpr size_t smem_bytes(bool grouped, bool pair) {
+  return 1024 /* alignment slack */ + (pair ? Cfg<true>::kTileBytes : Cfg<false>::kTileBytes) +
+         sizeof(SmemCtl) + (grouped ? 3 * (kMaxGroups + 1) * sizeof(int) : 0);
 }
 
 struct Tile {
-  int a_row;    // first row of A (and of C) covered by the tile
+  int a_row;    // first row of A (and of C) covered by the tile (first CTA of a pair)
   int row_end;  // rows >= row_end are not stored
   int b_row;    // first row of B (expert-offset for grouped)
   int n0;       // first output column
@@ -135,7 +160,7 @@ struct Tile {
 
 // Grouped tables in shared memory: s_lo[g] / s_hi[g] = clamped row range of
 // expert g, s_pre[g] = number of m-tiles of experts before g (s_pre[G] = all).
-template <bool kGrouped>
+template <bool kGrouped, int kTileM>
 __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_lo,
                                         const int *s_hi, const int *s_pre) {
   Tile r;
@@ -145,7 +170,7 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_l
     const int mt0 = band * kGroupM;
     const int rows = min(kGroupM, p.tiles_m - mt0);
     const int mt = mt0 + within % rows, nt = within / rows;
-    r.a_row = mt * BM;
+    r.a_row = mt * kTileM;
     r.row_end = p.M;
     r.n0 = nt * BN;
     r.b_row = r.n0;
@@ -162,7 +187,7 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_l
     const int mtiles = s_pre[g + 1] - s_pre[g];
     const int local = t - s_pre[g] * p.tiles_n;
     const int mt = local % mtiles, nt = local / mtiles;
-    r.a_row = s_lo[g] + mt * BM;
+    r.a_row = s_lo[g] + mt * kTileM;
     r.row_end = s_hi[g];
     r.n0 = nt * BN;
     r.b_row = g * p.N + r.n0;
@@ -171,33 +196,36 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_l
   return r;
 }
 
-template <int kBScale, bool kOutF32, bool kGrouped>
+template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8q_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmArgs p) {
+  using C = Cfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = smem + kStages * kABytes;
-  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + kTileBytes);
+  uint8_t *sB = smem + C::kStages * C::kABytes;
+  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + C::kTileBytes);
   int *s_lo = reinterpret_cast<int *>(ctl + 1);  // grouped only (see tile_of)
   int *s_hi = s_lo + (kMaxGroups + 1);
   int *s_prefix = s_hi + (kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int *abort_flag = &ctl->abort_flag;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0;  // 0 = the CTA that issues the MMAs
+  const int tile_first = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   // ---- set-up
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(smem_u32(&ctl->full[i]), 1);
       mbar_init(smem_u32(&ctl->empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->tfull[i]), 1);
-      mbar_init(smem_u32(&ctl->tempty[i]), kEpiWarps);
-      mbar_init(smem_u32(&ctl->sbfull[i]), kEpiWarps * 32);
+      mbar_init(smem_u32(&ctl->tempty[i]), C::kTemptyCount);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
@@ -208,10 +236,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    if (kPair) tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+    else tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
     tc_fence_before();
   }
-  __syncthreads();
+  // barriers initialised and TMEM allocated in every CTA before any CTA of the
+  // pair signals a peer
+  __syncwarp();
+  if (kPair) cluster_sync_all();
+  else __syncthreads();
   // grouped: clamp the expert offsets into [0, M] and build the m-tile prefix
   int total_tiles;
   if (kGrouped) {
@@ -227,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_lo[g] = lo;
         s_hi[g] = hi;
         s_prefix[g] = acc;
-        acc += (hi - lo + BM - 1) / BM;
+        acc += (hi - lo + C::kTileM - 1) / C::kTileM;
         prev_hi = hi;
       }
       s_prefix[p.G] = acc;
@@ -246,24 +279,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 4;
     const int quarter = warp & 3;        // TMEM lanes this warp may access
     const int col_base = (ew >> 2) * kEpiCols;  // this warp's columns of the 256
-    const int row_in_tile = quarter * 32 + lane;
+    const int row_in_tile = static_cast<int>(rank) * BM + quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int NB = (p.N + 127) / 128;
-    const int et = ew * 32 + lane;  // staging slot for per-column scales (< BN stages)
+    // the TMEM-empty barriers live in the MMA-issuing CTA
+    const uint32_t tempty_addr0 = kPair ? mapa_shared(smem_u32(&ctl->tempty[0]), 0)
+                                        : smem_u32(&ctl->tempty[0]);
+    const uint32_t tempty_addr1 = kPair ? mapa_shared(smem_u32(&ctl->tempty[1]), 0)
+                                        : smem_u32(&ctl->tempty[1]);
     int tb = 0;
     uint32_t tphase = 0;
     uint32_t sb_iter = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-      const Tile tl = tile_of<kGrouped>(t, p, s_lo, s_hi, s_prefix);
+    for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
+      const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_hi, s_prefix);
       const int m = tl.a_row + row_in_tile;
       const bool row_in = m < p.M;
       const int ncol0 = tl.n0 + col_base;
       const int nb = ncol0 / 128;
       const float *sb_g = p.sb;
       if (kGrouped) sb_g += static_cast<int64_t>(tl.g) * NB * p.num_kb;
-      // scales of K-group kb: sa of this row; sb of this warp's 128 columns
-      // (block kinds) or of column n0 + et (per-column kind, staged in smem)
+      // scales of K-group kb: sa of this row; sb of this warp's columns
+      // (block kinds: one value; per-column kind: lane l holds the 4 scales
+      // of columns 4l..4l+3 of the warp's kEpiCols, staged in shared memory)
       auto load_sa = [&](int kb) {
         return row_in ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ld_sa + m) : 0.0f;
       };
@@ -274,34 +312,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : 0.0f;
         if (kBScale == FP8Q_BSCALE_BLOCK_T)
           return nb < NB ? __ldg(p.sb + static_cast<int64_t>(kb) * p.ld_sb + nb) : 0.0f;
-        const int n = tl.n0 + et;
-        return (et < BN && n < p.N) ? __ldg(p.sb + static_cast<int64_t>(kb) * p.ld_sb + n) : 0.0f;
+        return 0.0f;
       };
+      auto load_sb4 = [&](int kb) {
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (kBScale == FP8Q_BSCALE_ROW) {
+          const int n = ncol0 + 4 * lane;
+          const float *src = p.sb + static_cast<int64_t>(kb) * p.ld_sb + n;
+          if (n + 0 < p.N) v.x = __ldg(src + 0);
+          if (n + 1 < p.N) v.y = __ldg(src + 1);
+          if (n + 2 < p.N) v.z = __ldg(src + 2);
+          if (n + 3 < p.N) v.w = __ldg(src + 3);
+        }
+        return v;
+      };
+      static_assert(kEpiCols == 4 * 32, "per-column scale staging assumes 4 columns per lane");
       uint64_t acc[kEpiCols / 2];  // packed FP32 pairs: columns (2i, 2i+1) of this thread's
 #pragma unroll
       for (int j = 0; j < kEpiCols / 2; ++j) acc[j] = 0ull;
       float sa_nx = p.num_kb > 0 ? load_sa(0) : 0.0f;
       float sb_nx = p.num_kb > 0 ? load_sb(0) : 0.0f;
+      float4 sb4_nx = p.num_kb > 0 ? load_sb4(0) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 
       for (int kb = 0; kb < p.num_kb; ++kb) {
         // the scales of group kb were loaded one iteration ago; fetch kb+1 now
         const float sa_v = sa_nx, sb_v = sb_nx;
+        const float4 sb4 = sb4_nx;
         if (kb + 1 < p.num_kb) {
           sa_nx = load_sa(kb + 1);
           sb_nx = load_sb(kb + 1);
+          sb4_nx = load_sb4(kb + 1);
         }
         if (kBScale == FP8Q_BSCALE_ROW) {
-          // per-column scales, staged through shared memory by all 256 threads
-          if (et < BN) ctl->sb_row[sb_iter & 1][et] = sb_v;
-          mbar_arrive(smem_u32(&ctl->sbfull[sb_iter & 1]));
-          // every lane waits; the warp then agrees (and reconverges) on the outcome
-          const bool got = mbar_wait_bounded(smem_u32(&ctl->sbfull[sb_iter & 1]),
-                                             (sb_iter >> 1) & 1, abort_flag, &g_status,
-                                             p.timeout_ns, FP8Q_ERR_TIMEOUT);
-          if (!__all_sync(0xffffffffu, got)) {
-            ok = false;
-            break;
-          }
+          // the buffer written here was last read two K-groups ago, before the
+          // previous iteration's __syncwarp
+          *reinterpret_cast<float4 *>(&ctl->sb_warp[ew][sb_iter & 1][4 * lane]) = sb4;
+          __syncwarp();
         }
         const uint64_t scale2 = pack_f32x2(sa_v * sb_v, sa_v * sb_v);
         const uint64_t sa2 = pack_f32x2(sa_v, sa_v);
@@ -320,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           if (kBScale == FP8Q_BSCALE_ROW) {
             const uint64_t *sbr =
-                reinterpret_cast<const uint64_t *>(&ctl->sb_row[sb_iter & 1][col_base + ch * 16]);
+                reinterpret_cast<const uint64_t *>(&ctl->sb_warp[ew][sb_iter & 1][ch * 16]);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               ffma2(acc[ch * 8 + j], pack_u32x2(r[2 * j], r[2 * j + 1]), fmul2(sbr[j], sa2));
@@ -332,14 +378,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[tb]));
+        if (lane == 0) {
+          if (kPair) mbar_arrive_cluster(tb ? tempty_addr1 : tempty_addr0);
+          else mbar_arrive(smem_u32(&ctl->tempty[tb]));
+        }
         tb ^= 1;
         if (tb == 0) tphase ^= 1;
         ++sb_iter;
       }
       if (!ok) break;
 
-      // ---- store the tile row (128 columns of row m)
+      // ---- store this thread's row segment (kEpiCols columns of row m)
       if (m < tl.row_end && ncol0 < p.N) {
         const bool full = ncol0 + kEpiCols <= p.N;
         if (kOutF32) {
@@ -347,12 +396,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kEpiCols; j += 4) {
             const float2 lo = unpack_f32x2(acc[j / 2]), hi = unpack_f32x2(acc[j / 2 + 1]);
+            float v[4] = {lo.x, lo.y, hi.x, hi.y};
             if (full || ncol0 + j + 4 <= p.N) {
-              *reinterpret_cast<float4 *>(crow + j) = make_float4(lo.x, lo.y, hi.x, hi.y);
+              if (kAccum) {  // C += result: one FP32 addition per element
+                const float4 old = *reinterpret_cast<const float4 *>(crow + j);
+                v[0] = __fadd_rn(old.x, v[0]);
+                v[1] = __fadd_rn(old.y, v[1]);
+                v[2] = __fadd_rn(old.z, v[2]);
+                v[3] = __fadd_rn(old.w, v[3]);
+              }
+              *reinterpret_cast<float4 *>(crow + j) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
-              const float v[4] = {lo.x, lo.y, hi.x, hi.y};
               for (int e = 0; e < 4; ++e)
-                if (ncol0 + j + e < p.N) crow[j + e] = v[e];
+                if (ncol0 + j + e < p.N) crow[j + e] = kAccum ? __fadd_rn(crow[j + e], v[e]) : v[e];
             }
           }
         } else {
@@ -382,7 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // teardown (epilogue side): TMEM reads are complete
     __syncwarp();
     tc_fence_before();
-    named_barrier_sync(1, kThreads);
+    if (kPair) cluster_sync_all();
+    else named_barrier_sync(1, kThreads);
     return;
   }
 
@@ -394,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_phase = 0;  // per-stage bit masks
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const Tile tl = tile_of<kGrouped>(t, p, s_lo, s_hi, s_prefix);
+      for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
+        const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_hi, s_prefix);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1, abort_flag, &g_status,
                                  p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
@@ -403,51 +460,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[stage]);
-          mbar_arrive_expect_tx(fb, kABytes + kBBytes);
-          tma_load_2d(smem_u32(sA + stage * kABytes), &tmA, fb, kb * BK, tl.a_row);
-          tma_load_2d(smem_u32(sB + stage * kBBytes), &tmB, fb, kb * BK, tl.b_row);
+          if (kPair) {
+            // both CTAs' copies complete on the MMA-issuing CTA's barrier, which
+            // expects the bytes of both
+            if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
+            const uint32_t fb0 = mapa_shared(fb, 0);
+            tma_load_2d_pair(smem_u32(sA + stage * C::kABytes), &tmA, fb0, kb * BK,
+                             tl.a_row + static_cast<int>(rank) * BM);
+            tma_load_2d_pair(smem_u32(sB + stage * C::kBBytes), &tmB, fb0, kb * BK,
+                             tl.b_row + static_cast<int>(rank) * (BN / 2));
+          } else {
+            mbar_arrive_expect_tx(fb, C::kTxBytes);
+            tma_load_2d(smem_u32(sA + stage * C::kABytes), &tmA, fb, kb * BK, tl.a_row);
+            tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmB, fb, kb * BK, tl.b_row);
+          }
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
       if (!ok) {
-        // drain: every armed stage's copy must land before the CTA exits
-        for (int s = 0; s < kStages; ++s)
-          if (armed & (1u << s)) mbar_wait_drain(smem_u32(&ctl->full[s]), (armed_phase >> s) & 1);
+        // drain: every armed stage's copy must land before the CTA exits (the
+        // MMA-issuing CTA's barriers see both CTAs' copies; a second CTA of a
+        // pair cannot wait on them and instead waits long enough for any copy)
+        if (!kPair || rank == 0) {
+          for (int s = 0; s < C::kStages; ++s)
+            if (armed & (1u << s))
+              mbar_wait_drain(smem_u32(&ctl->full[s]), (armed_phase >> s) & 1);
+        }
+        if (kPair) spin_ns(1000000);
       }
     }
   } else if (warp == 1) {
     // ================================================== MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int tb = 0;
       uint32_t tphase = 0;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&ctl->tempty[tb]), tphase ^ 1, abort_flag, &g_status,
-                                 p.timeout_ns, FP8Q_ERR_TIMEOUT) ||
+          // (in a pair the epilogues of both CTAs arrive here: cluster-scope acquire)
+          if (!mbar_wait_bounded<kPair>(smem_u32(&ctl->tempty[tb]), tphase ^ 1, abort_flag,
+                                        &g_status, p.timeout_ns, FP8Q_ERR_TIMEOUT) ||
               !mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_flag, &g_status,
                                  p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * kABytes));
-          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * C::kBBytes));
           const uint32_t d = tmem_base + static_cast<uint32_t>(tb * BN);
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&ctl->empty[stage]));
-          mma_commit(smem_u32(&ctl->tfull[tb]));
+          for (int k = 0; k < BK / 32; ++k) {
+            if (kPair) mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, C::kIdesc, k > 0 ? 1u : 0u);
+            else mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, C::kIdesc, k > 0 ? 1u : 0u);
+          }
+          if (kPair) {
+            mma_commit_pair_multicast(smem_u32(&ctl->empty[stage]), 0x3);
+            mma_commit_pair_multicast(smem_u32(&ctl->tfull[tb]), 0x3);
+          } else {
+            mma_commit(smem_u32(&ctl->empty[stage]));
+            mma_commit(smem_u32(&ctl->tfull[tb]));
+          }
           issued = true;
-          if (++stage == kStages) {
+          if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
           }
@@ -457,18 +539,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok && issued) {
         // drain: all MMAs issued so far must finish before TMEM is freed
-        mma_commit(smem_u32(&ctl->drain));
+        if (kPair) mma_commit_pair_multicast(smem_u32(&ctl->drain), 0x1);
+        else mma_commit(smem_u32(&ctl->drain));
         mbar_wait_drain(smem_u32(&ctl->drain), 0);
       }
     }
   }
-  // teardown (control side): wait for every warp, then free TMEM
+  // teardown (control side): wait for every warp (of both CTAs), then free TMEM
   __syncwarp();
   tc_fence_before();
-  named_barrier_sync(1, kThreads);
+  if (kPair) cluster_sync_all();
+  else named_barrier_sync(1, kThreads);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -489,80 +574,96 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns) {
 }
 
 // ------------------------------------------------------------------ host
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
 // 2-D byte tensor [rows][cols] with row pitch ld (bytes), box 128 x box_rows,
 // 128-byte swizzle, zero fill outside the tensor.
 bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint64_t ld,
                   uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {ld};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rows, cols, ld, 128, box_rows,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-std::atomic<uint64_t> g_timeout_ns{2000000000ull};
-
-template <int kBScale, bool kOutF32, bool kGrouped>
-fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args, int grid,
-                   cudaStream_t s) {
-  auto kern = fp8q_gemm_kernel<kBScale, kOutF32, kGrouped>;
-  static bool attr_set[kMaxDevices] = {};
+// Launch one instantiation.  `work_tiles` is the number of output tiles (an
+// upper bound for the grouped GEMM); the grid is persistent: one CTA (or one
+// CTA pair) per SM that can hold one, never more than there are tiles.
+template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false>
+fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
+                   int64_t work_tiles, cudaStream_t s) {
+  auto kern = fp8q_gemm_kernel<kBScale, kOutF32, kGrouped, kPair, kAccum>;
+  const size_t smem = smem_bytes(kGrouped, kPair);
+  static int max_units[kMaxDevices] = {};  // co-resident CTAs (or CTA pairs) per device
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (kPair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+  }
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (!attr_set[dev]) {
+    if (max_units[dev] == 0) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem_bytes(kGrouped))) != cudaSuccess)
+                               static_cast<int>(smem)) != cudaSuccess)
         return FP8Q_ERR_CUDA;
-      attr_set[dev] = true;
+      int n = 0;
+      if (kPair) {
+        cfg.gridDim = dim3(2, 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1)
+          return FP8Q_ERR_UNSUPPORTED;
+      } else {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+          return FP8Q_ERR_CUDA;
+      }
+      max_units[dev] = n;
     }
   }
-  kern<<<grid, kThreads, smem_bytes(kGrouped), s>>>(ta, tb, args);
+  const int64_t units = work_tiles < max_units[dev] ? work_tiles : max_units[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(units * (kPair ? 2 : 1)), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, args) != cudaSuccess) return FP8Q_ERR_CUDA;
   return launch_status();
+}
+
+// Tile shapes: kDensePair / kGroupedPair select CTA pairs (256 x 256 tiles)
+// or single CTAs (128 x 256 tiles) for the dense and grouped GEMMs.
+// C (FP32) += result: dense GEMMs only (gradient accumulation).
+fp8q_status dispatch_accumulate(int bkind, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const GemmArgs &a, int64_t tiles, cudaStream_t s) {
+  switch (bkind) {
+    case FP8Q_BSCALE_BLOCK:
+      return launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair, true>(ta, tb, a, tiles, s);
+    case FP8Q_BSCALE_BLOCK_T:
+      return launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair, true>(ta, tb, a, tiles, s);
+    default:
+      return launch<FP8Q_BSCALE_ROW, true, false, kDensePair, true>(ta, tb, a, tiles, s);
+  }
 }
 
 template <bool kGrouped>
 fp8q_status dispatch(int bkind, bool f32, const CUtensorMap &ta, const CUtensorMap &tb,
-                     const GemmArgs &a, int grid, cudaStream_t s) {
+                     const GemmArgs &a, int64_t tiles, cudaStream_t s) {
   if (kGrouped) {
-    return f32 ? launch<FP8Q_BSCALE_BLOCK, true, true>(ta, tb, a, grid, s)
-               : launch<FP8Q_BSCALE_BLOCK, false, true>(ta, tb, a, grid, s);
+    return f32 ? launch<FP8Q_BSCALE_BLOCK, true, true, kGroupedPair>(ta, tb, a, tiles, s)
+               : launch<FP8Q_BSCALE_BLOCK, false, true, kGroupedPair>(ta, tb, a, tiles, s);
   }
   switch (bkind) {
     case FP8Q_BSCALE_BLOCK:
-      return f32 ? launch<FP8Q_BSCALE_BLOCK, true, false>(ta, tb, a, grid, s)
-                 : launch<FP8Q_BSCALE_BLOCK, false, false>(ta, tb, a, grid, s);
+      return f32 ? launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair>(ta, tb, a, tiles, s)
+                 : launch<FP8Q_BSCALE_BLOCK, false, false, kDensePair>(ta, tb, a, tiles, s);
     case FP8Q_BSCALE_BLOCK_T:
-      return f32 ? launch<FP8Q_BSCALE_BLOCK_T, true, false>(ta, tb, a, grid, s)
-                 : launch<FP8Q_BSCALE_BLOCK_T, false, false>(ta, tb, a, grid, s);
+      return f32 ? launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair>(ta, tb, a, tiles, s)
+                 : launch<FP8Q_BSCALE_BLOCK_T, false, false, kDensePair>(ta, tb, a, tiles, s);
     default:
-      return f32 ? launch<FP8Q_BSCALE_ROW, true, false>(ta, tb, a, grid, s)
-                 : launch<FP8Q_BSCALE_ROW, false, false>(ta, tb, a, grid, s);
+      return f32 ? launch<FP8Q_BSCALE_ROW, true, false, kDensePair>(ta, tb, a, tiles, s)
+                 : launch<FP8Q_BSCALE_ROW, false, false, kDensePair>(ta, tb, a, tiles, s);
   }
 }
 
@@ -588,10 +689,10 @@ fp8q_status check_common(const void *a, int64_t lda, const void *b, int64_t ldb,
 
 using namespace fp8q;
 
-extern "C" fp8q_status fp8q_gemm(const void *a, int64_t lda, const float *sa, int64_t ld_sa,
-                                 const void *b, int64_t ldb, const float *sb, int64_t ld_sb,
-                                 int bscale_kind, void *c, int64_t ldc, int out_dtype, int64_t M,
-                                 int64_t N, int64_t K, void *stream) {
+static fp8q_status gemm_entry(const void *a, int64_t lda, const float *sa, int64_t ld_sa,
+                              const void *b, int64_t ldb, const float *sb, int64_t ld_sb,
+                              int bscale_kind, void *c, int64_t ldc, int out_dtype, int64_t M,
+                              int64_t N, int64_t K, void *stream, bool accumulate) {
   if (bscale_kind != FP8Q_BSCALE_BLOCK && bscale_kind != FP8Q_BSCALE_BLOCK_T &&
       bscale_kind != FP8Q_BSCALE_ROW)
     return FP8Q_ERR_INVALID;
@@ -607,13 +708,16 @@ extern "C" fp8q_status fp8q_gemm(const void *a, int64_t lda, const float *sa, in
   }
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  if (dev.max_smem_optin < static_cast<int>(smem_bytes(false))) return FP8Q_ERR_UNSUPPORTED;
+  if (dev.max_smem_optin < static_cast<int>(smem_bytes(false, kDensePair)))
+    return FP8Q_ERR_UNSUPPORTED;
   CUtensorMap ta, tb;
-  // K == 0: no loads happen; describe a dummy 1 x 128 tensor so the maps are valid
+  // K == 0: no loads happen; describe a dummy 1 x 128 tensor so the maps are valid.
+  // Each CTA of a pair loads 128 rows of A and 128 rows (half a tile) of B.
   const void *abase = K > 0 ? a : c;
   const void *bbase = K > 0 ? b : c;
   if (!make_tmap_u8(&ta, abase, K > 0 ? M : 1, K > 0 ? K : 128, K > 0 ? lda : 128, BM) ||
-      !make_tmap_u8(&tb, bbase, K > 0 ? N : 1, K > 0 ? K : 128, K > 0 ? ldb : 128, BN))
+      !make_tmap_u8(&tb, bbase, K > 0 ? N : 1, K > 0 ? K : 128, K > 0 ? ldb : 128,
+                    kDensePair ? BN / 2 : BN))
     return FP8Q_ERR_CUDA;
   GemmArgs args{};
   args.sa = sa;
@@ -625,16 +729,34 @@ extern "C" fp8q_status fp8q_gemm(const void *a, int64_t lda, const float *sa, in
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
   args.num_kb = static_cast<int>(KB);
-  args.tiles_m = static_cast<int>((M + BM - 1) / BM);
+  args.tiles_m = static_cast<int>((M + Cfg<kDensePair>::kTileM - 1) / Cfg<kDensePair>::kTileM);
   args.tiles_n = static_cast<int>((N + BN - 1) / BN);
   args.offs = nullptr;
   args.G = 0;
-  args.timeout_ns = g_timeout_ns.load();
+  args.timeout_ns = wait_timeout_ns().load();
   const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
   if (tiles >= (1ll << 31)) return FP8Q_ERR_SHAPE;
-  const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-  return dispatch<false>(bscale_kind, out_dtype == FP8Q_OUT_FP32, ta, tb, args, grid,
+  if (accumulate)
+    return dispatch_accumulate(bscale_kind, ta, tb, args, tiles, static_cast<cudaStream_t>(stream));
+  return dispatch<false>(bscale_kind, out_dtype == FP8Q_OUT_FP32, ta, tb, args, tiles,
                          static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8q_status fp8q_gemm(const void *a, int64_t lda, const float *sa, int64_t ld_sa,
+                                 const void *b, int64_t ldb, const float *sb, int64_t ld_sb,
+                                 int bscale_kind, void *c, int64_t ldc, int out_dtype, int64_t M,
+                                 int64_t N, int64_t K, void *stream) {
+  return gemm_entry(a, lda, sa, ld_sa, b, ldb, sb, ld_sb, bscale_kind, c, ldc, out_dtype, M, N, K,
+                    stream, false);
+}
+
+extern "C" fp8q_status fp8q_gemm_accumulate(const void *a, int64_t lda, const float *sa,
+                                            int64_t ld_sa, const void *b, int64_t ldb,
+                                            const float *sb, int64_t ld_sb, int bscale_kind,
+                                            float *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                            void *stream) {
+  return gemm_entry(a, lda, sa, ld_sa, b, ldb, sb, ld_sb, bscale_kind, c, ldc, FP8Q_OUT_FP32, M, N,
+                    K, stream, true);
 }
 
 extern "C" fp8q_status fp8q_grouped_gemm(const void *a, int64_t lda, const float *sa,
@@ -652,14 +774,15 @@ extern "C" fp8q_status fp8q_grouped_gemm(const void *a, int64_t lda, const float
   if (K > 0 && (!sb || !aligned4(sb))) return sb ? FP8Q_ERR_ALIGN : FP8Q_ERR_INVALID;
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  if (dev.max_smem_optin < static_cast<int>(smem_bytes(true))) return FP8Q_ERR_UNSUPPORTED;
+  if (dev.max_smem_optin < static_cast<int>(smem_bytes(true, kGroupedPair)))
+    return FP8Q_ERR_UNSUPPORTED;
   const int64_t KB = K / 128;
   CUtensorMap ta, tb;
   const void *abase = K > 0 ? a : c;
   const void *bbase = K > 0 ? b : c;
   if (!make_tmap_u8(&ta, abase, K > 0 ? M : 1, K > 0 ? K : 128, K > 0 ? lda : 128, BM) ||
       !make_tmap_u8(&tb, bbase, K > 0 ? static_cast<uint64_t>(G) * N : 1, K > 0 ? K : 128,
-                    K > 0 ? ldb : 128, BN))
+                    K > 0 ? ldb : 128, kGroupedPair ? BN / 2 : BN))
     return FP8Q_ERR_CUDA;
   GemmArgs args{};
   args.sa = sa;
@@ -671,16 +794,15 @@ extern "C" fp8q_status fp8q_grouped_gemm(const void *a, int64_t lda, const float
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
   args.num_kb = static_cast<int>(KB);
-  args.tiles_m = static_cast<int>((M + BM - 1) / BM);
+  args.tiles_m = static_cast<int>((M + Cfg<kGroupedPair>::kTileM - 1) / Cfg<kGroupedPair>::kTileM);
   args.tiles_n = static_cast<int>((N + BN - 1) / BN);
   args.offs = offs;
   args.G = G;
-  args.timeout_ns = g_timeout_ns.load();
+  args.timeout_ns = wait_timeout_ns().load();
   // upper bound on tiles: each expert adds at most one partial m-tile
   const int64_t bound = (static_cast<int64_t>(args.tiles_m) + G) * args.tiles_n;
   if (bound >= (1ll << 31)) return FP8Q_ERR_SHAPE;
-  const int grid = static_cast<int>(bound < dev.sm_count ? bound : dev.sm_count);
-  return dispatch<true>(FP8Q_BSCALE_BLOCK, out_dtype == FP8Q_OUT_FP32, ta, tb, args, grid,
+  return dispatch<true>(FP8Q_BSCALE_BLOCK, out_dtype == FP8Q_OUT_FP32, ta, tb, args, bound,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -693,11 +815,12 @@ extern "C" fp8q_status fp8q_sync_status(void *stream) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return FP8Q_ERR_CUDA;
   }
-  return static_cast<fp8q_status>(v);
+  const fp8q_status q = quant_status_take(s);
+  return v != 0 ? static_cast<fp8q_status>(v) : q;
 }
 
 extern "C" void fp8q_set_wait_timeout_ns(uint64_t ns) {
-  g_timeout_ns.store(ns ? ns : 2000000000ull);
+  wait_timeout_ns().store(ns ? ns : 2000000000ull);
 }
 
 extern "C" fp8q_status fp8q_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {

@@ -24,7 +24,32 @@
 #include "fp8q_ptx.cuh"
 
 namespace fp8q {
+
+// Device status word of the quantisers: 0, or FP8Q_ERR_TIMEOUT after one of
+// their bounded waits gave up (read and cleared by fp8q_sync_status()).
+__device__ int g_quant_status;
+
+fp8q_status quant_status_take(cudaStream_t s) {
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_quant_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_quant_status, &zero, sizeof(int)) != cudaSuccess) return FP8Q_ERR_CUDA;
+  }
+  return static_cast<fp8q_status>(v);
+}
+
 namespace {
+
+// Wait for a phase for at most 1 s regardless of any abort (own copies only).
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > 1000000000ull) return;
+}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 v;
@@ -108,57 +133,189 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
 // Both tile quantisers below load one 128 x 128 BF16 tile per CTA: 512
 // threads, a half-warp per 256-byte row, four rows per thread, 16-byte
 // non-caching loads.  The tile goes to shared memory as BF16 pairs, read back
-// by columns: thread (cp, tq) owns columns 2cp, 2cp+1 and rows 16tq..16tq+15.
+// by columns: for the column max-abs, thread (cp, tq) owns columns 2cp, 2cp+1
+// and rows 16tq..16tq+15; for the transposed codes, thread (c, q) owns column
+// c and rows 32q..32q+31 (one 32-byte sector of output).
 constexpr int kTileThreads = 512;
 
 // ------------------------------------------------------------------ 128x1
-// Grid (ceil(C / 128), T / 128).  Optionally quantises each row's 128
-// channels (1x128) from registers; then reduces each channel's max-abs over
-// the 128 tokens and writes each channel's 128 codes contiguously
-// (transposed output).
+// Persistent: each CTA walks 128-token x 128-channel tiles (channel blocks
+// fastest) with a two-deep shared-memory ring filled by TMA, so the next tile
+// streams in while this one is reduced and converted.  Per tile:
+//  - optionally the 1x128 codes of each row (half-warp per row, shuffles),
+//  - each channel's max-abs over the 128 tokens, its scale,
+//  - each channel's 128 codes written contiguously (transposed output).
+// Rows past C are zero-filled by TMA and never stored.
+constexpr uint32_t kTileBytesBF16 = 128 * 128 * 2;
+
 template <bool kPow2, bool kRows>
 __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
-    const uint16_t *__restrict__ x, int64_t C, int64_t ldx, uint8_t *__restrict__ qT, int64_t ldqT,
-    float *__restrict__ sT, int64_t ld_sT, uint8_t *__restrict__ q_rows, int64_t ldq_rows,
-    float *__restrict__ s_rows, int64_t ld_s_rows) {
-  __shared__ uint32_t tile[128][64];  // [token][channel pair], BF16x2 words
+    const __grid_constant__ CUtensorMap tmX, int64_t T, int64_t C, uint8_t *__restrict__ qT,
+    int64_t ldqT, float *__restrict__ sT, int64_t ld_sT, uint8_t *__restrict__ q_rows,
+    int64_t ldq_rows, float *__restrict__ s_rows, int64_t ld_s_rows, uint64_t timeout_ns) {
+  extern __shared__ uint8_t dsm_raw[];
+  auto tiles = reinterpret_cast<uint32_t(*)[128][64]>(
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ float red[8][128];
+  __shared__ float col_inv[128];
+  __shared__ uint64_t full[2];
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
+  const int64_t ncb = (C + 127) / 128;
+  const int64_t ntiles = ncb * (T / 128);
+  int pending[2] = {-1, -1};  // thread 0: parity of the copy in flight per buffer
+  if (tid == 0) {
+    mbar_init(smem_u32(&full[0]), 1);
+    mbar_init(smem_u32(&full[1]), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    for (int b = 0; b < 2; ++b) {
+      const int64_t t = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
+      if (t < ntiles) {
+        mbar_arrive_expect_tx(smem_u32(&full[b]), kTileBytesBF16);
+        tma_load_2d(smem_u32(&tiles[b][0][0]), &tmX, smem_u32(&full[b]),
+                    static_cast<int32_t>((t % ncb) * 128), static_cast<int32_t>((t / ncb) * 128));
+        pending[b] = 0;
+      }
+    }
+  }
+  __syncthreads();
+
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    const int buf = it & 1;
+    const bool got = mbar_wait_bounded(smem_u32(&full[buf]), (it >> 1) & 1, &abort_flag,
+                                       &g_quant_status, timeout_ns, FP8Q_ERR_TIMEOUT);
+    if (__syncthreads_or(!got)) {
+      if (tid == 0)  // let this CTA's own copies land before it exits
+        for (int b = 0; b < 2; ++b)
+          if (pending[b] >= 0) mbar_wait_drain(smem_u32(&full[b]), pending[b]);
+      return;
+    }
+    if (tid == 0) pending[buf] = -1;
+    uint32_t(*tile)[64] = tiles[buf];
+    const int64_t c0 = (t % ncb) * 128, t0 = (t / ncb) * 128;
+
+    if (kRows) {  // C % 128 == 0 here: every chunk is in range
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = hw + 32 * i;
+        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][l16 * 4]);
+        uint32_t mb = absmax_bits8(v);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+        float sc, inv;
+        group_scale(bits_to_f32_max(mb), kPow2, sc, inv);
+        *reinterpret_cast<uint2 *>(q_rows + (t0 + r) * ldq_rows + c0 + l16 * 8) = quantise8(v, inv);
+        if (l16 == 0) s_rows[(c0 / 128) * ld_s_rows + t0 + r] = sc;
+      }
+    }
+
+    const int cp = tid & 63, tq = tid >> 6;
+    uint32_t mw = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mw = umax16x2(mw, tile[tq * 16 + j][cp] & 0x7FFF7FFFu);
+    red[tq][2 * cp] = __uint_as_float(mw << 16);
+    red[tq][2 * cp + 1] = __uint_as_float(mw & 0xFFFF0000u);
+    __syncthreads();
+    if (tid < 128) {
+      float amax = red[0][tid];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i][tid]);
+      float sc, inv;
+      group_scale(amax, kPow2, sc, inv);
+      col_inv[tid] = inv;
+      if (c0 + tid < C) sT[(t0 / 128) * ld_sT + c0 + tid] = sc;
+    }
+    __syncthreads();
+
+    // transposed codes: thread (cc, tq4) owns channel c0 + cc and tokens
+    // 32 tq4 .. 32 tq4 + 31, i.e. one full 32-byte sector of that channel's row
+    const int cc = tid & 127, tq4 = tid >> 7;
+    const int64_t c = c0 + cc;
+    if (c < C) {
+      const float inv = col_inv[cc];
+      const int word = cc >> 1, shift = (cc & 1) ? 0 : 16;  // BF16 of channel cc in the word
+      uint32_t out[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          f[e] = __fmul_rn(
+              __uint_as_float((tile[tq4 * 32 + 4 * j + e][word] << shift) & 0xFFFF0000u), inv);
+        out[j] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(qT + c * ldqT + t0 + tq4 * 32);
+      dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+      dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+    __syncthreads();  // every thread is done with this buffer and col_inv
+    if (tid == 0) {
+      const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
+      if (tn < ntiles) {
+        // generic-proxy reads of the buffer above, async-proxy write below
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(smem_u32(&full[buf]), kTileBytesBF16);
+        tma_load_2d(smem_u32(&tile[0][0]), &tmX, smem_u32(&full[buf]),
+                    static_cast<int32_t>((tn % ncb) * 128), static_cast<int32_t>((tn / ncb) * 128));
+        pending[buf] = ((it + 2) >> 1) & 1;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ 128x1 from FP8
+// Grid (C / 128, T / 128).  Requantises FP8-cached activations: input E4M3
+// [T][C] with one 1x128 scale per (token, 128 channels), output the 128x1
+// codes transposed.  Each value is first dequantised with one FP32 multiply,
+// x = fl32(decode(q) * s_row), exactly as a BF16 input would be read; the
+// codes are decoded exactly (E4M3 is a subset of FP16) into shared memory.
+template <bool kPow2>
+__global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
+    const uint8_t *__restrict__ q, int64_t ldq, const float *__restrict__ s_rows,
+    int64_t ld_s_rows, uint8_t *__restrict__ qT, int64_t ldqT, float *__restrict__ sT,
+    int64_t ld_sT) {
+  __shared__ uint32_t tile[128][64];  // [token][channel pair], FP16x2 of the decoded codes
+  __shared__ float srow[128];
   __shared__ float red[8][128];
   __shared__ float col_inv[128];
 
   const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int64_t t0 = static_cast<int64_t>(blockIdx.y) * 128;
-  const bool chunk_ok = (c0 + l16 * 8) < C;  // C % 8 == 0: chunks are all-in or all-out
-
-  uint4 v[4];
+  if (tid < 128) srow[tid] = s_rows[blockIdx.x * ld_s_rows + t0 + tid];
+  uint2 raw[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    v[i] = make_uint4(0, 0, 0, 0);
-    if (chunk_ok) v[i] = ld_stream_v4(x + (t0 + hw + 32 * i) * ldx + c0 + l16 * 8);
-  }
-  if (kRows) {  // C % 128 == 0 here: every chunk is in range
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t t = t0 + hw + 32 * i;
-      uint32_t mb = absmax_bits8(v[i]);
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-      float s, inv;
-      group_scale(bits_to_f32_max(mb), kPow2, s, inv);
-      *reinterpret_cast<uint2 *>(q_rows + t * ldq_rows + c0 + l16 * 8) = quantise8(v[i], inv);
-      if (l16 == 0) s_rows[blockIdx.x * ld_s_rows + t] = s;
-    }
+    const uint8_t *src = q + (t0 + hw + 32 * i) * ldq + c0 + l16 * 8;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(raw[i].x), "=r"(raw[i].y)
+                 : "l"(src));
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4 *>(&tile[hw + 32 * i][l16 * 4]) = v[i];
+  for (int i = 0; i < 4; ++i) {
+    uint4 h;
+    h.x = decode_e4m3x2(static_cast<uint16_t>(raw[i].x & 0xFFFF));
+    h.y = decode_e4m3x2(static_cast<uint16_t>(raw[i].x >> 16));
+    h.z = decode_e4m3x2(static_cast<uint16_t>(raw[i].y & 0xFFFF));
+    h.w = decode_e4m3x2(static_cast<uint16_t>(raw[i].y >> 16));
+    *reinterpret_cast<uint4 *>(&tile[hw + 32 * i][l16 * 4]) = h;
+  }
   __syncthreads();
 
   const int cp = tid & 63, tq = tid >> 6;
-  uint32_t mw = 0;
+  float m_lo = 0.0f, m_hi = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) mw = umax16x2(mw, tile[tq * 16 + j][cp] & 0x7FFF7FFFu);
-  red[tq][2 * cp] = __uint_as_float(mw << 16);
-  red[tq][2 * cp + 1] = __uint_as_float(mw & 0xFFFF0000u);
+  for (int j = 0; j < 16; ++j) {
+    const int t = tq * 16 + j;
+    const uint32_t w = tile[t][cp];
+    m_lo = fmaxf(m_lo, fabsf(__fmul_rn(f16_lo(w), srow[t])));
+    m_hi = fmaxf(m_hi, fabsf(__fmul_rn(f16_hi(w), srow[t])));
+  }
+  red[tq][2 * cp] = m_lo;
+  red[tq][2 * cp + 1] = m_hi;
   __syncthreads();
   if (tid < 128) {
     float amax = red[0][tid];
@@ -167,28 +324,28 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
     float s, inv;
     group_scale(amax, kPow2, s, inv);
     col_inv[tid] = inv;
-    if (c0 + tid < C) sT[blockIdx.y * ld_sT + c0 + tid] = s;
+    sT[blockIdx.y * ld_sT + c0 + tid] = s;
   }
   __syncthreads();
 
-  const int64_t c = c0 + 2 * cp;
-  if (c < C) {  // c even, C % 8 == 0: c + 1 < C as well
-    const float inv_lo = col_inv[2 * cp], inv_hi = col_inv[2 * cp + 1];
-    uint32_t out_lo[4], out_hi[4];
+  const int cc = tid & 127, tq4 = tid >> 7;
+  const float inv = col_inv[cc];
+  uint32_t out[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t w0 = tile[tq * 16 + 4 * j + 0][cp], w1 = tile[tq * 16 + 4 * j + 1][cp];
-      const uint32_t w2 = tile[tq * 16 + 4 * j + 2][cp], w3 = tile[tq * 16 + 4 * j + 3][cp];
-      out_lo[j] = pack_e4m3x4(__fmul_rn(bf16_lo(w0), inv_lo), __fmul_rn(bf16_lo(w1), inv_lo),
-                              __fmul_rn(bf16_lo(w2), inv_lo), __fmul_rn(bf16_lo(w3), inv_lo));
-      out_hi[j] = pack_e4m3x4(__fmul_rn(bf16_hi(w0), inv_hi), __fmul_rn(bf16_hi(w1), inv_hi),
-                              __fmul_rn(bf16_hi(w2), inv_hi), __fmul_rn(bf16_hi(w3), inv_hi));
+  for (int j = 0; j < 8; ++j) {
+    float f[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = tq4 * 32 + 4 * j + e;
+      const uint32_t w = tile[t][cc >> 1];
+      const float x = __fmul_rn((cc & 1) ? f16_hi(w) : f16_lo(w), srow[t]);
+      f[e] = __fmul_rn(x, inv);
     }
-    *reinterpret_cast<uint4 *>(qT + c * ldqT + t0 + tq * 16) =
-        make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
-    *reinterpret_cast<uint4 *>(qT + (c + 1) * ldqT + t0 + tq * 16) =
-        make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+    out[j] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
   }
+  uint4 *dst = reinterpret_cast<uint4 *>(qT + (c0 + cc) * ldqT + t0 + tq4 * 32);
+  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
 // ------------------------------------------------------------------ 128x128
@@ -242,31 +399,93 @@ __global__ void __launch_bounds__(kTileThreads) quant_weight_kernel(
     if (n < N) *reinterpret_cast<uint2 *>(q + n * ldq + k0 + l16 * 8) = quantise8(v[i], inv);
   }
   if (kTrans) {
-    // thread (kp, nq): columns k0 + 2kp, k0 + 2kp + 1; rows n0 + 16nq .. + 15
-    const int kp = tid & 63, nq = tid >> 6;
-    uint32_t out_lo[4], out_hi[4];
+    // thread (kk, nq4): column k0 + kk, rows n0 + 32 nq4 .. + 31, i.e. one full
+    // 32-byte sector of row k0 + kk of the transposed codes
+    const int kk = tid & 127, nq4 = tid >> 7;
+    const int word = kk >> 1, shift = (kk & 1) ? 0 : 16;
+    uint32_t out[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t w0 = tile[nq * 16 + 4 * j + 0][kp], w1 = tile[nq * 16 + 4 * j + 1][kp];
-      const uint32_t w2 = tile[nq * 16 + 4 * j + 2][kp], w3 = tile[nq * 16 + 4 * j + 3][kp];
-      out_lo[j] = pack_e4m3x4(__fmul_rn(bf16_lo(w0), inv), __fmul_rn(bf16_lo(w1), inv),
-                              __fmul_rn(bf16_lo(w2), inv), __fmul_rn(bf16_lo(w3), inv));
-      out_hi[j] = pack_e4m3x4(__fmul_rn(bf16_hi(w0), inv), __fmul_rn(bf16_hi(w1), inv),
-                              __fmul_rn(bf16_hi(w2), inv), __fmul_rn(bf16_hi(w3), inv));
+    for (int j = 0; j < 8; ++j) {
+      float f[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        f[e] = __fmul_rn(__uint_as_float((tile[nq4 * 32 + 4 * j + e][word] << shift) & 0xFFFF0000u),
+                         inv);
+      out[j] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
     }
-    const int64_t nb0 = n0 + nq * 16;
-    uint8_t *row_lo = qT + (k0 + 2 * kp) * ldqT + nb0;
-    uint8_t *row_hi = qT + (k0 + 2 * kp + 1) * ldqT + nb0;
-    if (nb0 + 16 <= N) {
-      *reinterpret_cast<uint4 *>(row_lo) = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
-      *reinterpret_cast<uint4 *>(row_hi) = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+    const int64_t nb0 = n0 + nq4 * 32;
+    uint8_t *row = qT + (k0 + kk) * ldqT + nb0;
+    if (nb0 + 32 <= N) {
+      reinterpret_cast<uint4 *>(row)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+      reinterpret_cast<uint4 *>(row)[1] = make_uint4(out[4], out[5], out[6], out[7]);
     } else {
-      for (int j = 0; j < 16 && nb0 + j < N; ++j) {
-        row_lo[j] = static_cast<uint8_t>(out_lo[j >> 2] >> (8 * (j & 3)));
-        row_hi[j] = static_cast<uint8_t>(out_hi[j >> 2] >> (8 * (j & 3)));
-      }
+      for (int j = 0; j < 32 && nb0 + j < N; ++j)
+        row[j] = static_cast<uint8_t>(out[j >> 2] >> (8 * (j & 3)));
     }
   }
+}
+
+// ------------------------------------------------------------------ per tensor
+// Comparison path: one scale for a whole [M][K] tensor.  Two passes over a
+// workspace of one 32-bit partial per 64-row slab:
+//   pass 1: each CTA writes the packed max of |BF16| bits over its 64 rows;
+//   pass 2: each CTA reduces all partials to the tensor's max-abs, derives
+//           the scale (CTA 0 stores it) and quantises its 64 rows.
+constexpr int kTensorRows = 64;
+
+__global__ void __launch_bounds__(256) tensor_amax_kernel(const uint16_t *__restrict__ x,
+                                                          int64_t M, int64_t K, int64_t ldx,
+                                                          uint32_t *__restrict__ partials) {
+  __shared__ uint32_t warp_max[8];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTensorRows;
+  const int64_t r1 = r0 + kTensorRows < M ? r0 + kTensorRows : M;
+  const int64_t chunks = K / 8;  // 16-byte chunks per row
+  uint32_t mb = 0;
+  for (int64_t r = r0; r < r1; ++r)
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x)
+      mb = umax16x2(mb, absmax_bits8(ld_stream_v4(x + r * ldx + c * 8)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = mb;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t a = warp_max[0];
+    for (int i = 1; i < 8; ++i) a = umax16x2(a, warp_max[i]);
+    partials[blockIdx.x] = a;
+  }
+}
+
+template <bool kPow2>
+__global__ void __launch_bounds__(256) tensor_quant_kernel(const uint16_t *__restrict__ x,
+                                                           int64_t M, int64_t K, int64_t ldx,
+                                                           uint8_t *__restrict__ q, int64_t ldq,
+                                                           float *__restrict__ s_out,
+                                                           const uint32_t *__restrict__ partials,
+                                                           int n_partials) {
+  __shared__ uint32_t warp_max[8];
+  __shared__ float sh_inv;
+  uint32_t mb = 0;
+  for (int i = threadIdx.x; i < n_partials; i += blockDim.x) mb = umax16x2(mb, partials[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = mb;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t a = warp_max[0];
+    for (int i = 1; i < 8; ++i) a = umax16x2(a, warp_max[i]);
+    float sc, inv;
+    group_scale(bits_to_f32_max(a), kPow2, sc, inv);
+    sh_inv = inv;
+    if (blockIdx.x == 0) *s_out = sc;
+  }
+  __syncthreads();
+  const float inv = sh_inv;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTensorRows;
+  const int64_t r1 = r0 + kTensorRows < M ? r0 + kTensorRows : M;
+  const int64_t chunks = K / 8;
+  for (int64_t r = r0; r < r1; ++r)
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x)
+      *reinterpret_cast<uint2 *>(q + r * ldq + c * 8) = quantise8(ld_stream_v4(x + r * ldx + c * 8), inv);
 }
 
 // ------------------------------------------------------------------ cast
@@ -286,6 +505,33 @@ __global__ void __launch_bounds__(256) cast_e4m3_kernel(const float *__restrict_
 }
 
 bool valid_mode(int m) { return m == FP8Q_SCALE_FP32 || m == FP8Q_SCALE_POW2; }
+
+constexpr int kActTCtasPerSm = 3;  // 2 x 32 KB ring + 6 KB each: three fit per SM
+constexpr size_t kActTSmem = 2 * kTileBytesBF16 + 1024;
+
+template <bool kPow2, bool kRows>
+fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX, int64_t T,
+                         int64_t C, uint8_t *qT, int64_t ldqT, float *sT, int64_t ld_sT,
+                         uint8_t *q_rows, int64_t ldq_rows, float *s_rows, int64_t ld_s_rows,
+                         uint64_t timeout_ns) {
+  auto kern = quant_act_T_kernel<kPow2, kRows>;
+  static bool attr_set[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kActTSmem)) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+  }
+  kern<<<grid, kTileThreads, kActTSmem, s>>>(tmX, T, C, qT, ldqT, sT, ld_sT, q_rows, ldq_rows,
+                                             s_rows, ld_s_rows, timeout_ns);
+  return launch_status();
+}
 
 }  // namespace
 }  // namespace fp8q
@@ -333,25 +579,33 @@ extern "C" fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int
   if (rows && (!aligned16(q_rows) || !aligned4(s_rows) || ldq_rows % 16)) return FP8Q_ERR_ALIGN;
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  const dim3 grid(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>(T / 128));
+  CUtensorMap tmX;
+  if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(T),
+                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldx) * 2, 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+    return FP8Q_ERR_CUDA;
+  const int64_t ntiles = ((C + 127) / 128) * (T / 128);
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * kActTCtasPerSm;
+  const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
   auto s = static_cast<cudaStream_t>(stream);
-  auto xp = static_cast<const uint16_t *>(x);
   auto qp = static_cast<uint8_t *>(qT);
   auto rp = static_cast<uint8_t *>(q_rows);
+  const uint64_t tmo = wait_timeout_ns().load();
   const bool p2 = scale_mode == FP8Q_SCALE_POW2;
+  fp8q_status st = FP8Q_OK;
   if (p2 && rows)
-    quant_act_T_kernel<true, true>
-        <<<grid, kTileThreads, 0, s>>>(xp, C, ldx, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows, ld_s_rows);
+    st = launch_act_T<true, true>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+                                  ld_s_rows, tmo);
   else if (p2)
-    quant_act_T_kernel<true, false>
-        <<<grid, kTileThreads, 0, s>>>(xp, C, ldx, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows, ld_s_rows);
+    st = launch_act_T<true, false>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+                                   ld_s_rows, tmo);
   else if (rows)
-    quant_act_T_kernel<false, true>
-        <<<grid, kTileThreads, 0, s>>>(xp, C, ldx, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows, ld_s_rows);
+    st = launch_act_T<false, true>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+                                   ld_s_rows, tmo);
   else
-    quant_act_T_kernel<false, false>
-        <<<grid, kTileThreads, 0, s>>>(xp, C, ldx, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows, ld_s_rows);
-  return launch_status();
+    st = launch_act_T<false, false>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+                                    ld_s_rows, tmo);
+  return st;
 }
 
 extern "C" fp8q_status fp8q_quant_weight(const void *w, int64_t N, int64_t K, int64_t ldw,
@@ -401,5 +655,69 @@ extern "C" fp8q_status fp8q_cast_e4m3(const float *x, int64_t n, void *q, void *
   if (blocks > cap) blocks = cap;
   cast_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       x, n, static_cast<uint8_t *>(q));
+  return launch_status();
+}
+
+extern "C" fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, int64_t ldq,
+                                          const float *s_rows, int64_t ld_s_rows, void *qT,
+                                          int64_t ldqT, float *sT, int64_t ld_sT, int scale_mode,
+                                          void *stream) {
+  if (!valid_mode(scale_mode)) return FP8Q_ERR_INVALID;
+  if (T < 0 || C < 0 || T % 128 != 0 || C % 128 != 0 || ldq < C || ld_s_rows < T || ldqT < T ||
+      ld_sT < C)
+    return FP8Q_ERR_SHAPE;
+  if (T / 128 > 65535) return FP8Q_ERR_SHAPE;
+  if (T == 0 || C == 0) return FP8Q_OK;
+  if (!q || !s_rows || !qT || !sT) return FP8Q_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(qT) || !aligned4(s_rows) || !aligned4(sT) || ldq % 16 ||
+      ldqT % 16)
+    return FP8Q_ERR_ALIGN;
+  DeviceInfo dev;
+  if (fp8q_status st = device_info(dev)) return st;
+  const dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(T / 128));
+  auto s = static_cast<cudaStream_t>(stream);
+  auto qp = static_cast<const uint8_t *>(q);
+  auto tp = static_cast<uint8_t *>(qT);
+  if (scale_mode == FP8Q_SCALE_POW2)
+    requant_act_T_kernel<true><<<grid, kTileThreads, 0, s>>>(qp, ldq, s_rows, ld_s_rows, tp, ldqT,
+                                                             sT, ld_sT);
+  else
+    requant_act_T_kernel<false><<<grid, kTileThreads, 0, s>>>(qp, ldq, s_rows, ld_s_rows, tp,
+                                                              ldqT, sT, ld_sT);
+  return launch_status();
+}
+
+static int64_t tensor_partials(int64_t M) { return M > 0 ? (M + kTensorRows - 1) / kTensorRows : 1; }
+
+extern "C" int64_t fp8q_quant_tensor_workspace_bytes(int64_t M, int64_t K) {
+  (void)K;
+  return M < 0 ? 0 : tensor_partials(M) * static_cast<int64_t>(sizeof(uint32_t));
+}
+
+extern "C" fp8q_status fp8q_quant_tensor(const void *x, int64_t M, int64_t K, int64_t ldx, void *q,
+                                         int64_t ldq, float *s, void *workspace,
+                                         int64_t workspace_bytes, int scale_mode, void *stream) {
+  if (!valid_mode(scale_mode)) return FP8Q_ERR_INVALID;
+  if (M < 0 || K < 0 || K % 8 != 0 || ldx < K || ldq < K) return FP8Q_ERR_SHAPE;
+  const int64_t P = tensor_partials(M);
+  if (P > (1ll << 31) - 1) return FP8Q_ERR_SHAPE;
+  if (!s || !workspace) return FP8Q_ERR_INVALID;
+  if (workspace_bytes < P * static_cast<int64_t>(sizeof(uint32_t))) return FP8Q_ERR_SHAPE;
+  if (M > 0 && K > 0 && (!x || !q)) return FP8Q_ERR_INVALID;
+  if ((M > 0 && K > 0) && (!aligned16(x) || !aligned16(q) || ldx % 8 || ldq % 8))
+    return FP8Q_ERR_ALIGN;
+  if (!aligned4(s) || !aligned4(workspace)) return FP8Q_ERR_ALIGN;
+  DeviceInfo dev;
+  if (fp8q_status st = device_info(dev)) return st;
+  auto st_ = static_cast<cudaStream_t>(stream);
+  auto xp = static_cast<const uint16_t *>(x);
+  auto part = static_cast<uint32_t *>(workspace);
+  tensor_amax_kernel<<<static_cast<unsigned>(P), 256, 0, st_>>>(xp, M, K, ldx, part);
+  if (scale_mode == FP8Q_SCALE_POW2)
+    tensor_quant_kernel<true><<<static_cast<unsigned>(P), 256, 0, st_>>>(
+        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
+  else
+    tensor_quant_kernel<false><<<static_cast<unsigned>(P), 256, 0, st_>>>(
+        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
   return launch_status();
 }

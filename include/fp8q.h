@@ -106,6 +106,22 @@ fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int64_t ldx,
                              int64_t ld_s_rows, int scale_mode, void *stream);
 
 /*
+ * 128x1 requantisation of FP8-cached activations: the forward pass keeps its
+ * activations as 1x128-quantised E4M3 ([dssusan] paragraph 2: cached
+ * activations are stored in low precision), and the backward pass needs the
+ * same tensor in 128x1 tiles ([dssusan] paragraph 4).  Each cached value is
+ * dequantised with one FP32 multiply, x = fl32(decode(q[t][c]) * s_rows(t, c)),
+ * then quantised exactly as fp8q_quant_act_T quantises x.
+ *   q       E4M3 [T][ldq], columns [0, C).          T % 128 == 0, C % 128 == 0.
+ *   s_rows  FP32 1x128 scales of q: s_rows[(c/128) * ld_s_rows + t], ld_s_rows >= T.
+ *   qT      E4M3 [C][ldqT], qT[c][t];  sT FP32 sT[(t/128) * ld_sT + c].
+ * Alignment: q, qT 16-byte aligned; ldq % 16 == 0, ldqT % 16 == 0.
+ */
+fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, int64_t ldq,
+                               const float *s_rows, int64_t ld_s_rows, void *qT, int64_t ldqT,
+                               float *sT, int64_t ld_sT, int scale_mode, void *stream);
+
+/*
  * Weight quantisation, 128x128 blocks: one scale per 128 rows (output
  * channels) x 128 columns (input channels) ([dssusan] paragraph 4, Figure
  * 7 (a)(2)).  A last partial block of rows covers only the rows that exist.
@@ -121,6 +137,26 @@ fp8q_status fp8q_quant_weight(const void *w, int64_t N, int64_t K, int64_t ldw,
                               void *q, int64_t ldq, void *qT, int64_t ldqT,
                               float *sb, int64_t ld_sb, int scale_mode,
                               void *stream);
+
+/*
+ * Per-tensor quantisation, for comparison with the fine-grained quantisers:
+ * one scale for the whole tensor from its max-abs value, by the same rule as
+ * a group's.  This is the standard practice the pages contrast with the
+ * method ("Deepseek - Not For everyone", paragraph 4: mapping the tensor's
+ * max-abs onto the FP8 maximum makes the result sensitive to outliers).
+ * Two passes: per-64-row partial max-abs values go to `workspace`, then every
+ * slab reduces them and quantises.
+ *   x  BF16 [M][ldx], columns [0, K), K % 8 == 0;  q E4M3 [M][ldq];
+ *   s  one FP32 (device) -- the tensor's scale.
+ *   workspace  device scratch of at least fp8q_quant_tensor_workspace_bytes(M, K)
+ *              bytes, 4-byte aligned, owned by the caller; its contents on entry
+ *              do not matter.
+ * Alignment: x, q 16-byte aligned; ldx % 8, ldq % 8 == 0.
+ */
+int64_t fp8q_quant_tensor_workspace_bytes(int64_t M, int64_t K);
+fp8q_status fp8q_quant_tensor(const void *x, int64_t M, int64_t K, int64_t ldx,
+                              void *q, int64_t ldq, float *s, void *workspace,
+                              int64_t workspace_bytes, int scale_mode, void *stream);
 
 /*
  * FP8 GEMM with per-group scaling along K ([dssusan] paragraph 3, Figure 6;
@@ -145,6 +181,19 @@ fp8q_status fp8q_gemm(const void *a, int64_t lda, const float *sa,
                       const float *sb, int64_t ld_sb, int bscale_kind, void *c,
                       int64_t ldc, int out_dtype, int64_t M, int64_t N,
                       int64_t K, void *stream);
+
+/*
+ * Gradient accumulation form of fp8q_gemm: C += the same product, C FP32.
+ * Weight gradients are kept in FP32 and summed over micro-batches
+ * ([dssusan] paragraph 2: weight gradients stay in FP32); each element
+ * receives one FP32 addition, fl32(C_old + result).  Arguments and rules as
+ * fp8q_gemm with out_dtype = FP8Q_OUT_FP32.
+ */
+fp8q_status fp8q_gemm_accumulate(const void *a, int64_t lda, const float *sa,
+                                 int64_t ld_sa, const void *b, int64_t ldb,
+                                 const float *sb, int64_t ld_sb, int bscale_kind,
+                                 float *c, int64_t ldc, int64_t M, int64_t N,
+                                 int64_t K, void *stream);
 
 /*
  * Grouped FP8 GEMM for MoE experts: rows [offs[g], offs[g+1]) of A (tokens

@@ -84,6 +84,8 @@ def _load():
             L.oracle_bf16_gemm_rows.argtypes = [P, I64, P, I64, I64, I64, P, I64, P]
             L.oracle_requant_act_T.restype = None
             L.oracle_requant_act_T.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, INT]
+            L.oracle_quant_tensor.restype = None
+            L.oracle_quant_tensor.argtypes = [P, I64, I64, I64, P, I64, P, INT]
             L.oracle_num_threads.restype = INT
             L.oracle_num_threads.argtypes = []
             _lib = L
@@ -161,6 +163,16 @@ def quant_weight(w_bf16: np.ndarray, pow2: bool = False):
     sb = np.empty(((N + 127) // 128, K // 128), np.float32)
     _load().oracle_quant_weight(_ptr(w), N, K, K, _ptr(q), K, _ptr(sb), int(bool(pow2)))
     return q, sb
+
+
+def quant_tensor(x_bf16: np.ndarray, pow2: bool = False):
+    """Per-tensor quantisation (comparison only): x [M][K] -> q [M][K], one f32 scale."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.zeros(1, np.float32)
+    _load().oracle_quant_tensor(_ptr(x), M, K, K, _ptr(q), K, _ptr(s), int(bool(pow2)))
+    return q, s[0]
 
 
 def requant_act_T(q, s_rows, pow2: bool = False):

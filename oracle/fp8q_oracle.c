@@ -544,3 +544,26 @@ void oracle_requant_act_T(const uint8_t *q, int64_t T, int64_t C, int64_t ldq,
   par_for(C, requant_T_channel, p);
   free(p);
 }
+
+/* ------------------------------------------------------------------------
+ * Per-tensor quantisation, for comparison only: the standard practice the
+ * pages contrast with fine-grained scaling ("Deepseek - Not For everyone",
+ * paragraph 4: the max-abs of the whole tensor is mapped onto the largest FP8
+ * value, which makes the result sensitive to outliers).  One scale for the
+ * whole [M][K] tensor from its max-abs, by the same rule as a group's.
+ * ------------------------------------------------------------------------ */
+void oracle_quant_tensor(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
+                         int64_t ldq, float *s_out, int pow2) {
+  float amax = 0.0f;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t k = 0; k < K; ++k) {
+      float v = fabsf(bf16_to_f32(x[m * ldx + k]));
+      if (v > amax) amax = v;
+    }
+  float s, inv;
+  oracle_group_scale(amax, pow2, &s, &inv);
+  *s_out = s;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t k = 0; k < K; ++k)
+      q[m * ldq + k] = oracle_e4m3_encode(bf16_to_f32(x[m * ldx + k]) * inv);
+}

@@ -211,3 +211,39 @@ def test_wait_timeout_is_reported():
     B.fp8q_selftest_wait_timeout(2_000_000)   # 2 ms
     assert B.fp8q_sync_status() == B.FP8Q_ERR_TIMEOUT
     assert B.fp8q_sync_status() == 0          # cleared by the read
+
+
+def test_gemm_accumulate_wgrad_two_microbatches(oracle):
+    # dW accumulated over two micro-batches of tokens: dW = dY1^T X1 + dY2^T X2,
+    # FP32, each term a 128x1-quantised Wgrad GEMM (per-row scales)
+    T, d_in, d_out = 256, 264, 136
+    acc = torch.zeros((d_out, d_in), dtype=torch.float32, device="cuda")
+    ref = np.zeros((d_out, d_in))
+    absdot = np.zeros((d_out, d_in))
+    for mb in range(2):
+        dy = synth.normal_bf16((T, d_out), 1e-3, 40 + mb, "acc.dY")
+        x = synth.activation(T, d_in, seed=50 + mb, name="acc.X")
+        qdyT, sdyT = B.fp8q_quant_act_T(bf16_to_torch(dy))
+        qxT, sxT = B.fp8q_quant_act_T(bf16_to_torch(x))
+        B.fp8q_gemm_accumulate(qdyT, sdyT, qxT, sxT, acc, bscale_kind=B.FP8Q_BSCALE_ROW)
+        qdyT_r, sdyT_r = oracle.quant_act_T(dy)
+        qxT_r, sxT_r = oracle.quant_act_T(x)
+        r, ad = oracle.gemm_rows(qdyT_r, sdyT_r, qxT_r, sxT_r, oracle.BSCALE_ROW)
+        ref += r
+        absdot += ad
+    torch.cuda.synchronize()
+    # each accumulation adds one FP32 rounding of the running sum
+    tol = 2e-4 * absdot + 2 * np.abs(ref) * 2.0 ** -24
+    assert_within_tolerance(f64(acc), ref, tol, "accumulated wgrad")
+
+
+def test_gemm_accumulate_keeps_existing_values_for_k_zero():
+    M, N = 40, 136
+    c = torch.full((M, N), 1.5, dtype=torch.float32, device="cuda")
+    a = torch.empty((M, 0), dtype=torch.uint8, device="cuda")
+    b = torch.empty((N, 0), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((0, M), dtype=torch.float32, device="cuda")
+    sb = torch.empty((2, 0), dtype=torch.float32, device="cuda")
+    B.fp8q_gemm_accumulate(a, sa, b, sb, c)
+    torch.cuda.synchronize()
+    assert torch.all(c == 1.5)

@@ -170,3 +170,41 @@ def test_cast_exhaustive(oracle):
         nan = np.isnan(xs)
         assert np.all((got[nan] & 0x7F) == 0x7F), f"chunk {chunk}: NaN not kept"
         assert_bytes_equal(got[~nan], want[~nan], f"chunk {chunk}")
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("T,C", [(128, 128), (384, 256), (8192, 7168)])
+def test_requant_act_T_from_fp8_cache(oracle, T, C, pow2):
+    # the forward pass's cached 1x128 codes (FP32 or power-of-two scales) are
+    # requantised 128x1 for the backward pass
+    x = _special_rows(synth.activation(T, C, seed=500 + C))
+    q_r, s_r = oracle.quant_act(x, pow2)
+    qT_ref, sT_ref = oracle.requant_act_T(q_r, s_r, pow2)
+    q, s = B.fp8q_quant_act(bf16_to_torch(x), scale_mode=_mode(pow2))
+    qT, sT = B.fp8q_requant_act_T(q, s, scale_mode=_mode(pow2))
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(q), q_r, "cached codes")
+    assert_bytes_equal(u8(qT), qT_ref, "requantised codes")
+    assert_scales_equal(f32(sT), sT_ref, "requantised scales")
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("M,K", [(1, 8), (63, 200), (256, 1024), (4096, 7168)])
+def test_quant_tensor(oracle, M, K, pow2):
+    x = _special_rows(synth.activation(M, K, seed=600 + M)) if K >= 256 else \
+        synth.activation(M, K, seed=600 + M)
+    q_ref, s_ref = oracle.quant_tensor(x, pow2)
+    ws = torch.full((B.fp8q_quant_tensor_workspace_bytes(M, K),), 0xEE, dtype=torch.uint8,
+                    device="cuda")   # stale contents must not matter
+    q, s = B.fp8q_quant_tensor(bf16_to_torch(x), scale_mode=_mode(pow2), workspace=ws)
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(q), q_ref, "codes")
+    assert_scales_equal(f32(s), np.array([s_ref], np.float32), "tensor scale")
+
+
+def test_quant_tensor_workspace_too_small():
+    x = torch.zeros((200, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty((4,), dtype=torch.uint8, device="cuda")     # needs 4 partials
+    with pytest.raises(B.FP8QError) as e:
+        B.fp8q_quant_tensor(x, workspace=ws)
+    assert e.value.status == B.FP8Q_ERR_SHAPE

@@ -221,3 +221,45 @@ def test_requant_T_fp32_scales_invariants(oracle):
         if col[i] != 0:
             assert oracle.e4m3_decode(qT[c, i]) == np.copysign(448.0, col[i])
         assert sT[0, c] == np.float32(np.max(np.abs(deq[:, c]))) / np.float32(448.0)
+
+
+def test_quant_tensor_is_one_group(oracle):
+    # a single 1x128 group is a whole tensor: per-tensor and per-group agree
+    x = synth.activation(1, 128, seed=14)
+    for pow2 in (False, True):
+        q, s = oracle.quant_tensor(x, pow2)
+        qa, sa = oracle.quant_act(x, pow2)
+        assert np.array_equal(q, qa) and s == sa[0, 0]
+
+
+def test_quant_tensor_scale_is_max_of_group_scales(oracle):
+    # the tensor's scale is the largest 1x128 scale (monotone in max-abs), and
+    # groups holding the tensor's max-abs quantise identically
+    x = synth.activation(32, 512, seed=15)
+    q, s = oracle.quant_tensor(x)
+    qa, sa = oracle.quant_act(x)
+    assert s == sa.max()
+    g, m = np.unravel_index(np.argmax(sa), sa.shape)
+    assert np.array_equal(q[m, g * 128:(g + 1) * 128], qa[m, g * 128:(g + 1) * 128])
+
+
+def test_fine_grained_beats_per_tensor_on_outliers(oracle):
+    # the pages' motivation: with 0.1% x100 outliers, one scale for the whole
+    # tensor wastes precision on every other group; 1x128 scaling does not
+    x = synth.activation(256, 1024, seed=16)
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    q, s = oracle.quant_tensor(x)
+    qa, sa = oracle.quant_act(x)
+    err_t = oracle.e4m3_decode(q) * np.float64(s) - xf
+    err_g = oracle.e4m3_decode(qa) * np.repeat(sa.T.astype(np.float64), 128, axis=1) - xf
+    mse_t, mse_g = np.mean(err_t ** 2), np.mean(err_g ** 2)
+    assert mse_g < mse_t / 4
+
+
+def test_pow2_scale_of_infinite_max_abs(oracle):
+    # a dequantised FP8-cache value can overflow FP32 (E4M3 256 * 2^120 = 2^128);
+    # the exponent is then clamped to 127: s = 2^127, inv = 2^-127 (subnormal)
+    s, inv = oracle.group_scale(float("inf"), True)
+    assert s == np.float32(2.0 ** 127) and inv == np.float32(2.0 ** -127)
+    s, inv = oracle.group_scale(float("inf"), False)
+    assert np.isinf(s) and inv == 0.0
