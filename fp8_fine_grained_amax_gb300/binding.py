@@ -43,6 +43,7 @@ SIGNATURES = {
     "fp8q_requant_act_T": (_INT, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P]),
     "fp8q_quant_tensor_workspace_bytes": (_I64, [_I64, _I64]),
     "fp8q_quant_tensor": (_INT, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _I64, _INT, _P]),
+    "fp8q_quant_tensor_noalloc": (_INT, [_P, _I64, _I64, _I64, _P, _I64, _P, _INT, _P]),
     "fp8q_gemm": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P, _I64, _INT, _I64,
                          _I64, _I64, _P]),
     "fp8q_gemm_accumulate": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P, _I64, _I64,
@@ -211,6 +212,17 @@ def fp8q_quant_tensor(x, *, scale_mode=FP8Q_SCALE_FP32, q=None, s=None, workspac
         _ptr(x), M, K, _rows_ld(x, "x"), _ptr(q), _rows_ld(q, "q"), _ptr(s), _ptr(workspace),
         workspace.numel() * workspace.element_size(), scale_mode, _stream(stream)),
         "fp8q_quant_tensor")
+    return q, s
+
+
+def fp8q_quant_tensor_noalloc(x, q, s, *, scale_mode=FP8Q_SCALE_FP32, stream=None):
+    """fp8q_quant_tensor on the library's fixed per-device scratch: x BF16 [M][K]
+    (M <= 65536) into the caller's q uint8 [M][K] and s f32 [1].  Allocates
+    nothing; calls that overlap on the GPU share the scratch and race."""
+    M, K = x.shape
+    _check(load_library().fp8q_quant_tensor_noalloc(
+        _ptr(x), M, K, _rows_ld(x, "x"), _ptr(q), _rows_ld(q, "q"), _ptr(s), scale_mode,
+        _stream(stream)), "fp8q_quant_tensor_noalloc")
     return q, s
 
 

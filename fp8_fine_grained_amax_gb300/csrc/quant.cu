@@ -721,3 +721,63 @@ extern "C" fp8q_status fp8q_quant_tensor(const void *x, int64_t M, int64_t K, in
         xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
   return launch_status();
 }
+
+// ------------------------------------------------------------------ per tensor, no allocation
+// fp8q_quant_tensor without a caller-supplied workspace, for callers that
+// cannot allocate device memory at call time: code running inside an
+// allocator's or memory pool's own callbacks (allocating there would re-enter
+// the allocator), or a runtime that has handed all device memory to its own
+// pools and has none left to lend.  Its scratch is one fixed array per device
+// in the library's static device memory, sized for kNoAllocPartials partials
+// of kTensorRows rows each (M <= 65536).  Nothing in the array has to start at
+// zero: pass 1 writes every partial that pass 2 reads.  All calls on a device
+// share the array, so two of them that overlap on the GPU (different streams,
+// no ordering) race.
+constexpr int64_t kNoAllocPartials = 1024;  // 4 KB per device, held until the process exits
+static __device__ __align__(256) uint32_t g_noalloc_partials[kNoAllocPartials];
+
+// Device address of the array on the current device, looked up once per device.
+static fp8q_status noalloc_partials(uint32_t **out) {
+  static uint32_t *ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    uint32_t *ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_partials) != cudaSuccess ||
+        ptr == nullptr)
+      return FP8Q_ERR_CUDA;
+    ptrs[dev] = ptr;
+  }
+  *out = ptrs[dev];
+  return FP8Q_OK;
+}
+
+extern "C" fp8q_status fp8q_quant_tensor_noalloc(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                                 void *q, int64_t ldq, float *s, int scale_mode,
+                                                 void *stream) {
+  if (!valid_mode(scale_mode)) return FP8Q_ERR_INVALID;
+  if (M < 0 || K < 0 || K % 8 != 0 || ldx < K || ldq < K) return FP8Q_ERR_SHAPE;
+  const int64_t P = tensor_partials(M);
+  if (P > kNoAllocPartials) return FP8Q_ERR_SHAPE;
+  if (!s) return FP8Q_ERR_INVALID;
+  if (M > 0 && K > 0 && (!x || !q)) return FP8Q_ERR_INVALID;
+  if ((M > 0 && K > 0) && (!aligned16(x) || !aligned16(q) || ldx % 8 || ldq % 8))
+    return FP8Q_ERR_ALIGN;
+  if (!aligned4(s)) return FP8Q_ERR_ALIGN;
+  DeviceInfo dev;
+  if (fp8q_status st = device_info(dev)) return st;
+  uint32_t *part = nullptr;
+  if (fp8q_status st = noalloc_partials(&part)) return st;
+  auto st_ = static_cast<cudaStream_t>(stream);
+  auto xp = static_cast<const uint16_t *>(x);
+  tensor_amax_kernel<<<static_cast<unsigned>(P), 256, 0, st_>>>(xp, M, K, ldx, part);
+  if (scale_mode == FP8Q_SCALE_POW2)
+    tensor_quant_kernel<true><<<static_cast<unsigned>(P), 256, 0, st_>>>(
+        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
+  else
+    tensor_quant_kernel<false><<<static_cast<unsigned>(P), 256, 0, st_>>>(
+        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
+  return launch_status();
+}

@@ -159,6 +159,27 @@ fp8q_status fp8q_quant_tensor(const void *x, int64_t M, int64_t K, int64_t ldx,
                               int64_t workspace_bytes, int scale_mode, void *stream);
 
 /*
+ * fp8q_quant_tensor with no workspace argument and no allocation.  The
+ * sources describe no such call: it is a library convenience for callers that
+ * cannot allocate device memory when they quantise (code inside an
+ * allocator's or pool's callbacks, or a runtime whose device memory is all
+ * handed to its own pools).  The scratch is a fixed 4 KB array in the
+ * library's static device memory, one per device, so:
+ *   - M <= 65536 (1024 partials of 64 rows); larger M returns FP8Q_ERR_SHAPE
+ *     and launches nothing.  Every other argument, result and error is as for
+ *     fp8q_quant_tensor.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that call before any stream capture.
+ *   - Every call on a device uses the same array.  Calls whose kernels
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     and may return wrong scales; calls ordered on one stream do not.
+ * The call makes no cudaMalloc or cudaFree and allocates no other memory.
+ */
+fp8q_status fp8q_quant_tensor_noalloc(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                      void *q, int64_t ldq, float *s, int scale_mode,
+                                      void *stream);
+
+/*
  * FP8 GEMM with per-group scaling along K ([dssusan] paragraph 3, Figure 6;
  * [youlimart] paragraph 2):
  *   C[m][n] = sum over 128-wide groups kb of
