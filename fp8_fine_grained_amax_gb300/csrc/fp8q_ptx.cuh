@@ -54,35 +54,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same, with acquire semantics at cluster scope: for barriers that receive
-// arrivals from the other CTA of a pair.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait.  Returns true when the phase completed; false when the CTA's
 // abort flag is raised or `limit_ns` has passed (then it raises the abort
 // flag itself and records `code` in the device status word).
-template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort_flag,
                                                   int *status_word, uint64_t limit_ns,
                                                   int code) {
-  auto try_wait = [&]() {
-    return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-  };
-  if (try_wait()) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (try_wait()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
@@ -149,6 +131,28 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Wait for this thread's outstanding tcgen05.ld, with the given registers
+// passed through the wait: the loaded values are only defined after it, and
+// tying them to the instruction keeps their uses from being scheduled above it.
+__device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+// Ties more registers to the wait just issued (an empty volatile statement
+// that the compiler keeps in order after it).
+__device__ __forceinline__ void reg_tie(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
@@ -322,9 +326,12 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (may be the peer's).
+// Default (CTA-scope release) semantics: the only thing the arrive publishes is
+// that this CTA's tcgen05.ld of an accumulator has completed, which the
+// tcgen05.fence::before_thread_sync ahead of it already orders.  A
+// cluster-scope release here costs a full memory barrier on every K-group.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMEM allocation for a CTA pair (issued by one warp in each CTA of the pair).

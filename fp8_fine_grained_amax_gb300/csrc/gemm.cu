@@ -74,7 +74,7 @@ constexpr int kMaxGroups = 1024;
 constexpr uint64_t kDrainNs = 1000000000ull;  // 1 s for draining after an abort
 constexpr int kMaxStages = 6;
 constexpr bool kGroupedPair = false;  // tile shape of the grouped (MoE) GEMM
-constexpr bool kDensePair = false;    // tile shape of the dense GEMMs
+constexpr bool kDensePair = true;    // tile shape of the dense GEMMs
 
 // Two shapes of the same pipeline:
 //  single CTA: tile 128 x 256 per CTA; ring stage = A 128 rows + B 256 rows.
@@ -359,17 +359,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(tb * BN + col_base);
+        // TMEM loads in flight per wait: four for per-column scales, whose fold
+        // has more arithmetic per column to overlap with the next loads
+        constexpr int kLdBatch = kBScale == FP8Q_BSCALE_ROW ? 4 : 1;
+        uint32_t rbuf[kLdBatch][16];
 #pragma unroll
         for (int ch = 0; ch < kEpiCols / 16; ++ch) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + ch * 16, r);
-          tmem_wait_ld();
-          if (kBScale == FP8Q_BSCALE_ROW) {
-            const uint64_t *sbr =
-                reinterpret_cast<const uint64_t *>(&ctl->sb_warp[ew][sb_iter & 1][ch * 16]);
+          uint32_t(&r)[16] = rbuf[ch % kLdBatch];
+          if (kLdBatch == 1) {
+            tmem_ld_32x32b_x16(taddr + ch * 16, r);
+            tmem_wait_ld();
+          } else if (ch % kLdBatch == 0) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              ffma2(acc[ch * 8 + j], pack_u32x2(r[2 * j], r[2 * j + 1]), fmul2(sbr[j], sa2));
+            for (int b = 0; b < kLdBatch; ++b) tmem_ld_32x32b_x16(taddr + (ch + b) * 16, rbuf[b]);
+            tmem_wait_ld_tied(rbuf[0]);
+#pragma unroll
+            for (int b = 1; b < kLdBatch; ++b) reg_tie(rbuf[b]);
+          }
+          if (kBScale == FP8Q_BSCALE_ROW) {
+            // 16-byte shared loads: four column scales per broadcast read
+            const ulonglong2 *sbr =
+                reinterpret_cast<const ulonglong2 *>(&ctl->sb_warp[ew][sb_iter & 1][ch * 16]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const ulonglong2 sp = sbr[j];
+              ffma2(acc[ch * 8 + 2 * j], pack_u32x2(r[4 * j], r[4 * j + 1]), fmul2(sp.x, sa2));
+              ffma2(acc[ch * 8 + 2 * j + 1], pack_u32x2(r[4 * j + 2], r[4 * j + 3]),
+                    fmul2(sp.y, sa2));
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -504,9 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, issued = false;
       for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          // (in a pair the epilogues of both CTAs arrive here: cluster-scope acquire)
-          if (!mbar_wait_bounded<kPair>(smem_u32(&ctl->tempty[tb]), tphase ^ 1, abort_flag,
-                                        &g_status, p.timeout_ns, FP8Q_ERR_TIMEOUT) ||
+          // (in a pair the epilogues of both CTAs arrive here; their tcgen05.ld
+          // are ordered by the fences around the barrier, not by its scope)
+          if (!mbar_wait_bounded(smem_u32(&ctl->tempty[tb]), tphase ^ 1, abort_flag,
+                                 &g_status, p.timeout_ns, FP8Q_ERR_TIMEOUT) ||
               !mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_flag, &g_status,
                                  p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
             ok = false;
