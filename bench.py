@@ -230,10 +230,15 @@ class Workload:
 
 
 class Fprop(Workload):
-    def __init__(self, name, M, N, K):
-        self.name, self.M, self.N, self.K = name, M, N, K
+    """quant_act(X) + quant_weight(W) + GEMM.  pow2: power-of-two scales, and the
+    GEMM on the block-scaled MMA (fp8q_gemm_pow2)."""
+
+    def __init__(self, name, M, N, K, pow2=False):
+        self.name, self.M, self.N, self.K, self.pow2 = name, M, N, K, pow2
         self.config = {"M": M, "N": N, "K": K,
-                       "step": "quant_act(X) + quant_weight(W) + fp8_gemm -> bf16"}
+                       "step": ("quant_act(X, pow2) + quant_weight(W, pow2) + fp8_gemm_pow2 "
+                                "-> bf16") if pow2 else
+                               "quant_act(X) + quant_weight(W) + fp8_gemm -> bf16"}
 
     def host_inputs(self):
         from fp8_fine_grained_amax_gb300 import synth
@@ -258,16 +263,19 @@ class Fprop(Workload):
     def kernels(self, st, stream):
         from fp8_fine_grained_amax_gb300 import binding as B
         M, N, K = self.M, self.N, self.K
+        mode = B.FP8Q_SCALE_POW2 if self.pow2 else B.FP8Q_SCALE_FP32
+        gemm = B.fp8q_gemm_pow2 if self.pow2 else B.fp8q_gemm
         return [
             Kernel("quant_act_kernel",
-                   lambda: B.fp8q_quant_act(st["X"], q=st["qa"], sa=st["sa"], stream=stream),
+                   lambda: B.fp8q_quant_act(st["X"], q=st["qa"], sa=st["sa"], scale_mode=mode,
+                                            stream=stream),
                    M * K * 2 + M * K + (K // 128) * M * 4, "hbm"),
             Kernel("quant_weight_kernel",
-                   lambda: B.fp8q_quant_weight(st["W"], q=st["qb"], sb=st["sb"], stream=stream),
+                   lambda: B.fp8q_quant_weight(st["W"], q=st["qb"], sb=st["sb"], scale_mode=mode,
+                                               stream=stream),
                    N * K * 3 + ((N + 127) // 128) * (K // 128) * 4, "hbm"),
-            Kernel("fp8q_gemm_kernel",
-                   lambda: B.fp8q_gemm(st["qa"], st["sa"], st["qb"], st["sb"], c=st["C"],
-                                       stream=stream),
+            Kernel("fp8q_gemm_mx_kernel" if self.pow2 else "fp8q_gemm_kernel",
+                   lambda: gemm(st["qa"], st["sa"], st["qb"], st["sb"], c=st["C"], stream=stream),
                    2.0 * M * N * K, "tensor"),
         ]
 
@@ -275,10 +283,10 @@ class Fprop(Workload):
         import oracle
         M, N, K = self.M, self.N, self.K
         t0 = time.perf_counter()
-        qa, sa = oracle.quant_act(inp["X"])
+        qa, sa = oracle.quant_act(inp["X"], self.pow2)
         t_act = time.perf_counter() - t0
         t0 = time.perf_counter()
-        qb, sb = oracle.quant_weight(inp["W"])
+        qb, sb = oracle.quant_weight(inp["W"], self.pow2)
         t_w = time.perf_counter() - t0
         rows, t_g = _sampled_rows(
             lambda r: oracle.gemm_rows(qa, sa, qb, sb, oracle.BSCALE_BLOCK, r), M,
@@ -292,12 +300,14 @@ class Fprop(Workload):
 class LinearBwd(Workload):
     """Backward of Y = X W^T with X [T][d_in], W [d_out][d_in], dY [T][d_out]."""
 
-    def __init__(self, T=8192, d_in=7168, d_out=2048):
-        self.name = f"linear_bwd_T{T}"
-        self.T, self.d_in, self.d_out = T, d_in, d_out
+    def __init__(self, T=8192, d_in=7168, d_out=2048, pow2=False):
+        self.name = f"linear_bwd_pow2_T{T}" if pow2 else f"linear_bwd_T{T}"
+        self.T, self.d_in, self.d_out, self.pow2 = T, d_in, d_out, pow2
         self.config = {"T": T, "d_in": d_in, "d_out": d_out,
                        "step": "quant_act_T(dY, fused 1x128) + quant_act_T(X) + "
-                               "quant_weight(W, transposed) + Dgrad (bf16) + Wgrad (fp32)"}
+                               "quant_weight(W, transposed) + Dgrad (bf16) + Wgrad (fp32)" +
+                               (", power-of-two scales, GEMMs on the block-scaled MMA"
+                                if pow2 else "")}
 
     def host_inputs(self):
         from fp8_fine_grained_amax_gb300 import synth
@@ -326,21 +336,25 @@ class LinearBwd(Workload):
     def kernels(self, st, stream):
         from fp8_fine_grained_amax_gb300 import binding as B
         T, di, do = self.T, self.d_in, self.d_out
+        mode = B.FP8Q_SCALE_POW2 if self.pow2 else B.FP8Q_SCALE_FP32
+        gemm = B.fp8q_gemm_pow2 if self.pow2 else B.fp8q_gemm
+        gname = "fp8q_gemm_mx_kernel" if self.pow2 else "fp8q_gemm_kernel"
         return [
             Kernel("quant_act_T_kernel(dY,rows)", lambda: B.fp8q_quant_act_T(
                 st["dY"], with_rows=True, qT=st["qdyT"], sT=st["sdyT"], q_rows=st["qdy"],
-                s_rows=st["sdy"], stream=stream), T * do * 4 + (T // 128) * do * 4 +
-                (do // 128) * T * 4, "hbm"),
+                s_rows=st["sdy"], scale_mode=mode, stream=stream), T * do * 4 +
+                (T // 128) * do * 4 + (do // 128) * T * 4, "hbm"),
             Kernel("quant_act_T_kernel(X)", lambda: B.fp8q_quant_act_T(
-                st["X"], qT=st["qxT"], sT=st["sxT"], stream=stream),
+                st["X"], qT=st["qxT"], sT=st["sxT"], scale_mode=mode, stream=stream),
                 T * di * 3 + (T // 128) * di * 4, "hbm"),
             Kernel("quant_weight_kernel(T)", lambda: B.fp8q_quant_weight(
                 st["W"], with_transpose=True, q=st["qw"], qT=st["qwT"], sb=st["sw"],
-                stream=stream), do * di * 4 + (do // 128) * (di // 128) * 4, "hbm"),
-            Kernel("fp8q_gemm_kernel(dgrad)", lambda: B.fp8q_gemm(
+                scale_mode=mode, stream=stream), do * di * 4 + (do // 128) * (di // 128) * 4,
+                "hbm"),
+            Kernel(gname + "(dgrad)", lambda: gemm(
                 st["qdy"], st["sdy"], st["qwT"], st["sw"], bscale_kind=B.FP8Q_BSCALE_BLOCK_T,
                 c=st["dX"], stream=stream), 2.0 * T * di * do, "tensor"),
-            Kernel("fp8q_gemm_kernel(wgrad)", lambda: B.fp8q_gemm(
+            Kernel(gname + "(wgrad)", lambda: gemm(
                 st["qdyT"], st["sdyT"], st["qxT"], st["sxT"], bscale_kind=B.FP8Q_BSCALE_ROW,
                 out_dtype=B.FP8Q_OUT_FP32, c=st["dW"], stream=stream), 2.0 * do * di * T,
                 "tensor"),
@@ -350,10 +364,11 @@ class LinearBwd(Workload):
         import oracle
         T, di, do = self.T, self.d_in, self.d_out
         t0 = time.perf_counter()
-        qdyT, sdyT = oracle.quant_act_T(inp["dY"])
-        qdy, sdy = oracle.quant_act(inp["dY"])
-        qxT, sxT = oracle.quant_act_T(inp["X"])
-        qw, sw = oracle.quant_weight(inp["W"])
+        p2 = self.pow2
+        qdyT, sdyT = oracle.quant_act_T(inp["dY"], p2)
+        qdy, sdy = oracle.quant_act(inp["dY"], p2)
+        qxT, sxT = oracle.quant_act_T(inp["X"], p2)
+        qw, sw = oracle.quant_weight(inp["W"], p2)
         qwT = np.ascontiguousarray(qw.T)
         t_q = time.perf_counter() - t0
         budget = (target_s - t_q) / 2
@@ -583,6 +598,10 @@ def _sampled_rows(run, M, budget_s):
 def make_workload(name: str) -> Workload:
     if name == "fprop_4096x7168x7168":
         return Fprop(name, 4096, 7168, 7168)
+    if name == "fprop_pow2_4096x7168x7168":
+        return Fprop(name, 4096, 7168, 7168, pow2=True)
+    if name == "linear_bwd_pow2_T8192":
+        return LinearBwd(pow2=True)
     if name == "tiny_fprop":
         return Fprop(name, 256, 256, 512)
     if name.startswith("square_"):

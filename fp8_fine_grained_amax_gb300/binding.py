@@ -48,6 +48,10 @@ SIGNATURES = {
                          _I64, _I64, _P]),
     "fp8q_gemm_accumulate": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P, _I64, _I64,
                                     _I64, _I64, _P]),
+    "fp8q_gemm_pow2": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P, _I64, _INT, _I64,
+                         _I64, _I64, _P]),
+    "fp8q_gemm_pow2_accumulate": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _INT, _P, _I64, _I64,
+                                    _I64, _I64, _P]),
     "fp8q_grouped_gemm": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _INT, _P, _I64, _INT,
                                  _I64, _I64, _I64, _P]),
     "fp8q_cast_e4m3": (_INT, [_P, _I64, _P, _P]),
@@ -227,7 +231,7 @@ def fp8q_quant_tensor_noalloc(x, q, s, *, scale_mode=FP8Q_SCALE_FP32, stream=Non
 
 
 def fp8q_gemm(a, sa, b, sb, *, bscale_kind=FP8Q_BSCALE_BLOCK, out_dtype=FP8Q_OUT_BF16, c=None,
-              stream=None):
+              stream=None, _entry="fp8q_gemm"):
     """C [M][N] = per-128-K-group scaled a [M][K] x b [N][K]^T (E4M3 codes)."""
     M, K = a.shape
     N = b.shape[0]
@@ -236,14 +240,23 @@ def fp8q_gemm(a, sa, b, sb, *, bscale_kind=FP8Q_BSCALE_BLOCK, out_dtype=FP8Q_OUT
         c = torch.empty((M, N), dtype=dt, device=a.device)
     ld_sa = _rows_ld(sa, "sa") if sa.numel() else M
     ld_sb = _rows_ld(sb, "sb") if sb.numel() else 1
-    _check(load_library().fp8q_gemm(
+    _check(getattr(load_library(), _entry)(
         _ptr(a), _rows_ld(a, "a") if a.numel() else K, _ptr(sa), ld_sa, _ptr(b),
         _rows_ld(b, "b") if b.numel() else K, _ptr(sb), ld_sb, bscale_kind, _ptr(c),
-        _rows_ld(c, "c"), out_dtype, M, N, K, _stream(stream)), "fp8q_gemm")
+        _rows_ld(c, "c"), out_dtype, M, N, K, _stream(stream)), _entry)
     return c
 
 
-def fp8q_gemm_accumulate(a, sa, b, sb, c, *, bscale_kind=FP8Q_BSCALE_BLOCK, stream=None):
+def fp8q_gemm_pow2(a, sa, b, sb, *, bscale_kind=FP8Q_BSCALE_BLOCK, out_dtype=FP8Q_OUT_BF16,
+                   c=None, stream=None):
+    """fp8q_gemm for power-of-two scales (FP8Q_SCALE_POW2 quantisers) on the
+    block-scaled MMA; same arguments and result."""
+    return fp8q_gemm(a, sa, b, sb, bscale_kind=bscale_kind, out_dtype=out_dtype, c=c,
+                     stream=stream, _entry="fp8q_gemm_pow2")
+
+
+def fp8q_gemm_accumulate(a, sa, b, sb, c, *, bscale_kind=FP8Q_BSCALE_BLOCK, stream=None,
+                         _entry="fp8q_gemm_accumulate"):
     """c (FP32 [M][N]) += per-128-K-group scaled a [M][K] x b [N][K]^T."""
     M, K = a.shape
     N = b.shape[0]
@@ -251,11 +264,17 @@ def fp8q_gemm_accumulate(a, sa, b, sb, c, *, bscale_kind=FP8Q_BSCALE_BLOCK, stre
         raise ValueError("c must be an FP32 [M][N] tensor")
     ld_sa = _rows_ld(sa, "sa") if sa.numel() else M
     ld_sb = _rows_ld(sb, "sb") if sb.numel() else 1
-    _check(load_library().fp8q_gemm_accumulate(
+    _check(getattr(load_library(), _entry)(
         _ptr(a), _rows_ld(a, "a") if a.numel() else K, _ptr(sa), ld_sa, _ptr(b),
         _rows_ld(b, "b") if b.numel() else K, _ptr(sb), ld_sb, bscale_kind, _ptr(c),
-        _rows_ld(c, "c"), M, N, K, _stream(stream)), "fp8q_gemm_accumulate")
+        _rows_ld(c, "c"), M, N, K, _stream(stream)), _entry)
     return c
+
+
+def fp8q_gemm_pow2_accumulate(a, sa, b, sb, c, *, bscale_kind=FP8Q_BSCALE_BLOCK, stream=None):
+    """c (FP32 [M][N]) += the fp8q_gemm_pow2 product."""
+    return fp8q_gemm_accumulate(a, sa, b, sb, c, bscale_kind=bscale_kind, stream=stream,
+                                _entry="fp8q_gemm_pow2_accumulate")
 
 
 def fp8q_grouped_gemm(a, sa, b, sb, offs, *, out_dtype=FP8Q_OUT_BF16, c=None, stream=None):

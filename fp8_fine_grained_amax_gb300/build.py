@@ -25,7 +25,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8q.so")
-SOURCES = ["gemm.cu", "quant.cu", "api.cu"]
+SOURCES = ["gemm.cu", "gemm_mx.cu", "quant.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -68,12 +68,12 @@ def launch_regs_of(gemm_src: str) -> int:
     return int(m.group(1))
 
 
-def check_gemm_registers(ptxas_log: str, expected: int) -> None:
-    """Every fp8q_gemm_kernel instantiation must be built for `expected` registers."""
+def check_gemm_registers(ptxas_log: str, expected: int, kernel: str = "fp8q_gemm_kernel") -> None:
+    """Every instantiation of `kernel` must be built for `expected` registers."""
     entries = re.split(r"Compiling entry function", ptxas_log)
     found = 0
     for e in entries:
-        if "fp8q_gemm_kernel" not in e.split("\n", 1)[0]:
+        if kernel not in e.split("\n", 1)[0]:
             continue
         m = re.search(r"Used (\d+) registers", e)
         if not m or int(m.group(1)) != expected:
@@ -82,7 +82,7 @@ def check_gemm_registers(ptxas_log: str, expected: int) -> None:
                 "setmaxnreg split would not balance" % (expected, m and m.group(0)))
         found += 1
     if found == 0:
-        raise RuntimeError("ptxas report names no fp8q_gemm_kernel")
+        raise RuntimeError("ptxas report names no " + kernel)
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:
@@ -93,6 +93,8 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         results = dict(zip(SOURCES, ex.map(_compile, SOURCES)))
     check_gemm_registers(results["gemm.cu"][1], launch_regs_of(os.path.join(CSRC, "gemm.cu")))
+    check_gemm_registers(results["gemm_mx.cu"][1], launch_regs_of(os.path.join(CSRC, "gemm_mx.cu")),
+                         "fp8q_gemm_mx_kernel")
     if verbose:
         for src, (_, log) in results.items():
             print(f"== {src}\n{log}")

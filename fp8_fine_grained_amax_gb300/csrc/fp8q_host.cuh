@@ -98,5 +98,7 @@ inline bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *b
 
 // Read (and clear) the quantisers' device status word; defined in quant.cu.
 fp8q_status quant_status_take(cudaStream_t s);
+// The same for the power-of-two (block-scaled MMA) GEMM; defined in gemm_mx.cu.
+fp8q_status mx_status_take(cudaStream_t s);
 
 }  // namespace fp8q

@@ -41,12 +41,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// True once the phase with the given parity has completed.
+// True once the phase with the given parity has completed.  The suspend-time
+// hint (1 us) lets the hardware park the waiting thread until the phase
+// completes instead of returning at once; the callers' loops still bound the
+// total wait.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -378,6 +381,64 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void *
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar_cluster_addr)
       : "memory");
+}
+
+}  // namespace fp8q
+
+namespace fp8q {
+
+// ---------------------------------------------------------------- block-scaled MMA
+// tcgen05.mma ... kind::mxf8f6f4.block_scale.scale_vec::1X: each 32-wide K
+// block of a row of A and of a row of B carries an unsigned 8-bit power-of-two
+// exponent (UE8M0, bias 127, 255 = NaN) held in tensor memory.  Layout in TMEM
+// (established by a probe with single-instruction, exactly representable
+// results): the scale of row r of A (r < 128, per CTA) is at lane r, column
+// sfa + r/32; the scale of row n of B (n < 256) is at column sfb + n/32 of
+// lane 32*(r/32) + n%32 for the D rows r it multiplies, i.e. replicated in
+// each 32-lane quarter.  The byte within the 32-bit cell is selected by the
+// instruction descriptor's scale-factor ids, so one cell can carry four
+// consecutive K blocks' exponents.  The same layout holds in each CTA of a
+// pair (each CTA holds its own rows' A scales and all of the tile's B scales).
+
+// Instruction descriptor for kind::mxf8f6f4 with UE8M0 scales: A, B E4M3
+// K-major, D FP32 (implied), shape M x N; a_id / b_id pick the scale byte.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, uint32_t a_id, uint32_t b_id) {
+  return (b_id << 4)                                 // B scale-factor byte
+         | (0u << 7) | (0u << 10)                    // A, B: E4M3
+         | (0u << 15) | (0u << 16)                   // A, B K-major
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale type UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+         | (a_id << 29);                             // A scale-factor byte
+}
+
+// D[tmem of both CTAs] (+)= (A . 2^sfa) * (B . 2^sfb)^T, M = 256 across the pair.
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Register -> TMEM stores: thread i of the warp writes lane (base lane + i),
+// 1 or 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 }  // namespace fp8q

@@ -834,7 +834,9 @@ extern "C" fp8q_status fp8q_sync_status(void *stream) {
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return FP8Q_ERR_CUDA;
   }
   const fp8q_status q = quant_status_take(s);
-  return v != 0 ? static_cast<fp8q_status>(v) : q;
+  const fp8q_status x = mx_status_take(s);
+  if (v != 0) return static_cast<fp8q_status>(v);
+  return q != FP8Q_OK ? q : x;
 }
 
 extern "C" void fp8q_set_wait_timeout_ns(uint64_t ns) {

@@ -1,0 +1,663 @@
+// gemm_mx.cu -- the per-group-scaled FP8 GEMM for power-of-two scales, on the
+// tensor cores' block-scaled MMA (sm_103a).
+//
+//   C[m][n] = sum_kb 2^ea(m,kb) * 2^eb(n,kb) * sum_{k in kb} a[m][k] * b[n][k]
+//
+// With the method's power-of-two scaling factors (dssusan.co.kr post 91437,
+// paragraph 1) every scale is 2^e, and the pages' recommendation that tensor
+// cores take the group scales themselves (same post, paragraph 3) is what
+// Blackwell's microscaling MMA does ("Deepseek - Not For everyone",
+// paragraph 3): tcgen05.mma kind::mxf8f6f4.block_scale multiplies each
+// 32-wide K block of A and B by 2^e (UE8M0 exponents held in tensor memory)
+// inside the MMA.  The 128-wide group's exponent is used for its four K
+// blocks.  Products of powers of two are exact, so the result is the same
+// product as the FP32-scale path's, accumulated over the whole K in the FP32
+// TMEM accumulator with no per-group fold by the CUDA cores.
+//
+// Roles (384 threads; CTA pairs, tile 256 x 256, one MMA thread per pair):
+//   warp 0      TMA producer: this CTA's 128 rows of A and 128 rows of B per
+//               K-group into a kStages ring, completing on the leading CTA's
+//               "full" barrier.
+//   warp 1      MMA issuer (leading CTA): per K-group 4 x tcgen05.mma
+//               .cta_group::2 .kind::mxf8f6f4 .block_scale (M=256, N=256,
+//               K=32) into one TMEM accumulator (columns 0-255), reading the
+//               scale exponents of the current scale stage.
+//   warps 4-11  scale producers and epilogue.  Scale stage s (TMEM columns
+//               256 + 16 s .. +15, 16 stages) holds the exponents of four
+//               consecutive K-groups, one byte per group: warps 4-7 write the
+//               A exponents of their rows (column +q for lane quarter q),
+//               warps 8-11 the B exponents of the tile's 256 columns (columns
+//               +8..+15, the same in every lane quarter).  After the last
+//               K-group of a tile they read the accumulator (each thread 128
+//               columns of its row), release it, and store C.
+//
+// The epilogue runs up to 16 scale stages (64 K-groups) ahead of the MMA
+// within a tile and into the next tile before draining the current one, so
+// the only pause of the tensor cores between tiles is the accumulator read.
+// A scale that is not a power of two (2^-127 .. 2^127) is a caller error: the
+// kernel uses its exponent and records FP8Q_ERR_INVALID in its status word.
+// Every wait is bounded in time (as in the FP32-scale GEMM).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "fp8q.h"
+#include "fp8q_host.cuh"
+#include "fp8q_ptx.cuh"
+
+namespace fp8q {
+
+// Device status word of this kernel (read and cleared by fp8q_sync_status).
+__device__ int g_mx_status;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int kTileM = 2 * BM;                  // C rows per pair tile
+constexpr int kStages = 6;                      // operand ring depth
+constexpr uint32_t kABytes = BM * BK;           // per CTA per stage
+constexpr uint32_t kBBytes = (BN / 2) * BK;     // per CTA per stage (half the columns)
+constexpr uint32_t kTxBytes = 2 * (kABytes + kBBytes);
+constexpr size_t kRingBytes = static_cast<size_t>(kStages) * (kABytes + kBBytes);
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 128 + kEpiWarps * 32;
+constexpr int kLaunchRegs = 168;                // must match ptxas' count (checked by the build)
+constexpr int kCtlRegs = 40, kEpiRegs = 232;
+static_assert(kCtlRegs + 2 * kEpiRegs <= 3 * kLaunchRegs, "register split must fit the launch");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = BN;               // accumulator: columns [0, 256)
+constexpr int kSfStages = 16;                   // scale stages: columns [256, 512)
+constexpr uint32_t kSfStageCols = 16;
+constexpr uint32_t kSfbOffset = 8;              // B exponents at +8..+15 of a stage
+static_assert(kAccCols + kSfStages * kSfStageCols <= kTmemCols, "TMEM budget");
+constexpr int kGroupsPerStage = 4;              // one byte per K-group in a 32-bit cell
+constexpr int kRunAhead = 6;                    // stages of the next tile written before a drain
+static_assert(kRunAhead < kSfStages, "run-ahead must not wait on the next tile's MMAs");
+constexpr int kGroupM = 16;                     // L2 rasterisation band (m-tiles)
+constexpr uint64_t kDrainNs = 1000000000ull;
+
+struct MxArgs {
+  const float *sa;
+  int64_t ld_sa;
+  const float *sb;
+  int64_t ld_sb;
+  void *c;
+  int64_t ldc;
+  int M, N;
+  int num_kb;
+  int tiles_m, tiles_n;
+  uint64_t timeout_ns;
+};
+
+struct alignas(8) MxCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t sfull[kSfStages];   // leading CTA: scale stage written (16 warp arrivals)
+  uint64_t sempty[kSfStages];  // every CTA: scale stage consumed by the MMAs
+  uint64_t tfull;              // every CTA: accumulator complete
+  uint64_t tempty;             // leading CTA: accumulator read (16 warp arrivals)
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(MxCtl);
+
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kDrainNs) return;
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
+// UE8M0 exponent byte of a power-of-two FP32 scale; `bad` is set for any other
+// value (the exponent field is then used, clamped below the NaN code).
+__device__ __forceinline__ uint32_t ue8m0_of(float s, bool &bad) {
+  const uint32_t b = __float_as_uint(s);
+  if (b == 0x00400000u) return 0u;  // 2^-127, the one subnormal power of two in range
+  const uint32_t e = (b >> 23) & 0xFFu;
+  if ((b & 0x807FFFFFu) != 0u || e == 0u || e == 0xFFu) bad = true;
+  return e < 0xFFu ? e : 0xFEu;
+}
+
+struct MxTile {
+  int m0;  // first row of the pair tile
+  int n0;  // first column
+};
+
+__device__ __forceinline__ MxTile mx_tile_of(int t, const MxArgs &p) {
+  const int band_tiles = kGroupM * p.tiles_n;
+  const int band = t / band_tiles, within = t - band * band_tiles;
+  const int mt0 = band * kGroupM;
+  const int rows = min(kGroupM, p.tiles_m - mt0);
+  MxTile r;
+  r.m0 = (mt0 + within % rows) * kTileM;
+  r.n0 = (within / rows) * BN;
+  return r;
+}
+
+template <int kBScale, bool kOutF32, bool kAccum>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8q_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const MxArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + kStages * kABytes;
+  MxCtl *ctl = reinterpret_cast<MxCtl *>(smem + kRingBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int *abort_flag = &ctl->abort_flag;
+  const uint32_t rank = cluster_ctarank();  // 0 = the CTA that issues the MMAs
+  const int tile_first = static_cast<int>(blockIdx.x >> 1);
+  const int tile_step = static_cast<int>(gridDim.x >> 1);
+  const int total_tiles = p.tiles_m * p.tiles_n;
+  const int nst = (p.num_kb + kGroupsPerStage - 1) / kGroupsPerStage;  // scale stages per tile
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&ctl->full[i]), 1);
+      mbar_init(smem_u32(&ctl->empty[i]), 1);
+    }
+    for (int i = 0; i < kSfStages; ++i) {
+      mbar_init(smem_u32(&ctl->sfull[i]), 2 * kEpiWarps);
+      mbar_init(smem_u32(&ctl->sempty[i]), 1);
+    }
+    mbar_init(smem_u32(&ctl->tfull), 1);
+    mbar_init(smem_u32(&ctl->tempty), 2 * kEpiWarps);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+    tc_fence_before();
+  }
+  __syncwarp();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp >= 4) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+    // ================================================== scale producers + epilogue
+    const int ew = warp - 4;
+    const int q = warp & 3;          // lane quarter this warp may access
+    const bool a_side = ew < 4;      // warps 4-7: A exponents; 8-11: B exponents
+    const int col_half = ew >> 2;    // epilogue: columns [128 * col_half, +128)
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
+    const uint32_t sfull0 = mapa_shared(smem_u32(&ctl->sfull[0]), 0);
+    const uint32_t tempty0 = mapa_shared(smem_u32(&ctl->tempty), 0);
+    int ss = 0;           // next scale stage slot to write
+    uint32_t sphase = 0;  // its phase
+    uint32_t tphase = 0;
+    bool ok = true;
+
+    // Scale production walks a cursor over (tile, stage) in the order the MMA
+    // consumes stages.  The raw FP32 scales of the stage at the cursor were
+    // loaded one stage earlier: a global load takes about a microsecond under
+    // the GEMM's own L2 traffic, as long as the tensor cores take to consume a
+    // stage, so loading them at use would put that latency on the critical path.
+    //   A warps: raw[0..3] = sa of this thread's row, K-groups 4 js .. 4 js + 3.
+    //   B warps, per-column scales: raw[4 c + j] = sb of column n0 + 32 c + lane.
+    //   B warps, block scales: raw[4 h + j] = the scale of 128-column block h.
+    constexpr int kRaw = kBScale == FP8Q_BSCALE_ROW ? 32 : 8;
+    const int NB = (p.N + 127) / 128;
+    auto load_raw = [&](int t, int js, float (&r)[kRaw]) {
+      const MxTile tl = mx_tile_of(t, p);
+      const int kb0 = js * kGroupsPerStage;
+#pragma unroll
+      for (int i = 0; i < kRaw; ++i) r[i] = 1.0f;
+      if (a_side) {
+        const int m = tl.m0 + row_in_tile;
+#pragma unroll
+        for (int j = 0; j < kGroupsPerStage; ++j)
+          if (kb0 + j < p.num_kb && m < p.M)
+            r[j] = __ldg(p.sa + static_cast<int64_t>(kb0 + j) * p.ld_sa + m);
+      } else if (kBScale == FP8Q_BSCALE_ROW) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int n = tl.n0 + 32 * c + lane;
+#pragma unroll
+          for (int j = 0; j < kGroupsPerStage; ++j)
+            if (kb0 + j < p.num_kb && n < p.N)
+              r[4 * c + j] = __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + n);
+        }
+      } else {
+        // columns past N in a partial block read zero-filled B rows, so the
+        // block's own scale is as good as any for them
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int nb = tl.n0 / 128 + h;
+#pragma unroll
+          for (int j = 0; j < kGroupsPerStage; ++j)
+            if (kb0 + j < p.num_kb && nb < NB)
+              r[4 * h + j] = kBScale == FP8Q_BSCALE_BLOCK
+                                 ? __ldg(p.sb + static_cast<int64_t>(nb) * p.ld_sb + kb0 + j)
+                                 : __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + nb);
+        }
+      }
+    };
+    float raw[kRaw];
+    int cur_t = tile_first, cur_js = 0;  // production cursor
+    if (cur_t < total_tiles) load_raw(cur_t, 0, raw);
+
+    // Write the stage at the cursor into slot ss and advance the cursor.
+    auto produce = [&]() -> bool {
+      int nt = cur_t, njs = cur_js + 1;
+      if (njs == nst) {
+        nt += tile_step;
+        njs = 0;
+      }
+      float nxt[kRaw];
+      if (nt < total_tiles) load_raw(nt, njs, nxt);
+      const bool got = mbar_wait_bounded(smem_u32(&ctl->sempty[ss]), sphase ^ 1, abort_flag,
+                                         &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, got)) return false;  // tcgen05.st needs the whole warp
+      tc_fence_after();
+      const uint32_t col = kAccCols + static_cast<uint32_t>(ss) * kSfStageCols;
+      bool bad = false;
+      if (a_side) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int j = 0; j < kGroupsPerStage; ++j) w |= ue8m0_of(raw[j], bad) << (8 * j);
+        tmem_st_32x32b_x1(tmem_base + lane_addr + col + static_cast<uint32_t>(q), w);
+      } else {
+        uint32_t w[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int base = kBScale == FP8Q_BSCALE_ROW ? 4 * c : 4 * (c / 4);
+          uint32_t word = 0;
+#pragma unroll
+          for (int j = 0; j < kGroupsPerStage; ++j) word |= ue8m0_of(raw[base + j], bad) << (8 * j);
+          w[c] = word;
+        }
+        tmem_st_32x32b_x8(tmem_base + lane_addr + col + kSfbOffset, w);
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(&g_mx_status, 0, FP8Q_ERR_INVALID);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(sfull0 + static_cast<uint32_t>(ss) * 8u);
+      if (++ss == kSfStages) {
+        ss = 0;
+        sphase ^= 1;
+      }
+#pragma unroll
+      for (int i = 0; i < kRaw; ++i) raw[i] = nxt[i];
+      cur_t = nt;
+      cur_js = njs;
+      return true;
+    };
+
+    for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
+      const MxTile tl = mx_tile_of(t, p);
+      while (ok && cur_t == t) ok = produce();  // the rest of this tile's stages
+      // run ahead into the next tile, enough stages to cover the drain and the
+      // stores below.  Stage js of the next tile reuses the slot of this
+      // tile's stage js + nst - kSfStages, so a short run-ahead finishes well
+      // before this tile's last MMAs and never delays the drain; it must also
+      // stay under kSfStages, or a wait would depend on the next tile's own
+      // MMAs (which need the drain).
+      const int lim = nst < kRunAhead ? nst : kRunAhead;
+      while (ok && cur_t == t + tile_step && cur_t < total_tiles && cur_js < lim) ok = produce();
+      if (!ok) break;
+
+      // ---- drain the accumulator: this thread's row, 128 columns
+      const bool got = mbar_wait_bounded(smem_u32(&ctl->tfull), tphase, abort_flag,
+                                         &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tphase ^= 1;
+      tc_fence_after();
+      uint32_t v[8][16];
+      const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(col_half * 128);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tmem_ld_32x32b_x16(taddr + (4 * h + b) * 16, v[4 * h + b]);
+        tmem_wait_ld_tied(v[4 * h]);
+#pragma unroll
+        for (int b = 1; b < 4; ++b) reg_tie(v[4 * h + b]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0);
+
+      // ---- store C
+      const int m = tl.m0 + row_in_tile;
+      const int ncol0 = tl.n0 + col_half * 128;
+      if (m < p.M && ncol0 < p.N) {
+        const bool full = ncol0 + 128 <= p.N;
+        if (kOutF32) {
+          float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
+#pragma unroll
+          for (int j = 0; j < 128; j += 4) {
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(v[(j + e) / 16][(j + e) % 16]);
+            if (full || ncol0 + j + 4 <= p.N) {
+              if (kAccum) {
+                const float4 old = *reinterpret_cast<const float4 *>(crow + j);
+                x[0] = __fadd_rn(old.x, x[0]);
+                x[1] = __fadd_rn(old.y, x[1]);
+                x[2] = __fadd_rn(old.z, x[2]);
+                x[3] = __fadd_rn(old.w, x[3]);
+              }
+              *reinterpret_cast<float4 *>(crow + j) = make_float4(x[0], x[1], x[2], x[3]);
+            } else {
+              for (int e = 0; e < 4; ++e)
+                if (ncol0 + j + e < p.N) crow[j + e] = kAccum ? __fadd_rn(crow[j + e], x[e]) : x[e];
+            }
+          }
+        } else {
+          __nv_bfloat16 *crow =
+              static_cast<__nv_bfloat16 *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
+#pragma unroll
+          for (int j = 0; j < 128; j += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c0 = j + 2 * e;
+              __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[c0 / 16][c0 % 16]),
+                                                       __uint_as_float(v[c0 / 16][c0 % 16 + 1]));
+              w[e] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            if (full || ncol0 + j + 8 <= p.N) {
+              *reinterpret_cast<uint4 *>(crow + j) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              for (int e = 0; e < 8; ++e)
+                if (ncol0 + j + e < p.N)
+                  reinterpret_cast<uint16_t *>(crow)[j + e] =
+                      static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
+    return;
+  }
+
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+  if (warp == 0) {
+    // ================================================== TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
+        const MxTile tl = mx_tile_of(t, p);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1, abort_flag,
+                                 &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[stage]);
+          if (rank == 0) mbar_arrive_expect_tx(fb, kTxBytes);
+          const uint32_t fb0 = mapa_shared(fb, 0);
+          tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmA, fb0, kb * BK,
+                           tl.m0 + static_cast<int>(rank) * BM);
+          tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &tmB, fb0, kb * BK,
+                           tl.n0 + static_cast<int>(rank) * (BN / 2));
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        if (rank == 0) {
+          for (int s = 0; s < kStages; ++s)
+            if (armed & (1u << s)) mbar_wait_drain(smem_u32(&ctl->full[s]), (armed_phase >> s) & 1);
+        }
+        spin_ns(1000000);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================== MMA issuer
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int ss = 0;
+      uint32_t sphase = 0;
+      uint32_t tphase = 0;
+      bool ok = true, issued = false;
+      for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
+        // the accumulator must have been read out (both CTAs)
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty), tphase ^ 1, abort_flag, &g_mx_status,
+                               p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
+          ok = false;
+          break;
+        }
+        tphase ^= 1;
+        tc_fence_after();
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          const uint32_t j = static_cast<uint32_t>(kb % kGroupsPerStage);
+          if (j == 0) {
+            if (!mbar_wait_bounded(smem_u32(&ctl->sfull[ss]), sphase, abort_flag, &g_mx_status,
+                                   p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_flag, &g_mx_status,
+                                 p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * kABytes));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+          const uint32_t sfa = tmem_base + kAccCols + static_cast<uint32_t>(ss) * kSfStageCols;
+          const uint32_t idesc = idesc_mx_e4m3(kTileM, BN, j, j);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_mx_pair(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, sfa, sfa + kSfbOffset,
+                        (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair_multicast(smem_u32(&ctl->empty[stage]), 0x3);
+          if (j == kGroupsPerStage - 1 || kb == p.num_kb - 1) {
+            mma_commit_pair_multicast(smem_u32(&ctl->sempty[ss]), 0x3);
+            if (++ss == kSfStages) {
+              ss = 0;
+              sphase ^= 1;
+            }
+          }
+          issued = true;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_multicast(smem_u32(&ctl->tfull), 0x3);
+      }
+      if (!ok && issued) {
+        mma_commit_pair_multicast(smem_u32(&ctl->drain), 0x1);
+        mbar_wait_drain(smem_u32(&ctl->drain), 0);
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+template <int kBScale, bool kOutF32, bool kAccum>
+fp8q_status launch_mx(const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs &args,
+                      int64_t tiles, cudaStream_t s) {
+  auto kern = fp8q_gemm_mx_kernel<kBScale, kOutF32, kAccum>;
+  static int max_pairs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // CTA pairs
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (max_pairs[dev] == 0) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+      int n = 0;
+      cfg.gridDim = dim3(2, 1, 1);
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1)
+        return FP8Q_ERR_UNSUPPORTED;
+      max_pairs[dev] = n;
+    }
+  }
+  const int64_t pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, args) != cudaSuccess) return FP8Q_ERR_CUDA;
+  return launch_status();
+}
+
+template <bool kAccum>
+fp8q_status dispatch_mx(int bkind, bool f32, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const MxArgs &a, int64_t tiles, cudaStream_t s) {
+  if (kAccum) {
+    switch (bkind) {
+      case FP8Q_BSCALE_BLOCK: return launch_mx<FP8Q_BSCALE_BLOCK, true, true>(ta, tb, a, tiles, s);
+      case FP8Q_BSCALE_BLOCK_T:
+        return launch_mx<FP8Q_BSCALE_BLOCK_T, true, true>(ta, tb, a, tiles, s);
+      default: return launch_mx<FP8Q_BSCALE_ROW, true, true>(ta, tb, a, tiles, s);
+    }
+  }
+  switch (bkind) {
+    case FP8Q_BSCALE_BLOCK:
+      return f32 ? launch_mx<FP8Q_BSCALE_BLOCK, true, false>(ta, tb, a, tiles, s)
+                 : launch_mx<FP8Q_BSCALE_BLOCK, false, false>(ta, tb, a, tiles, s);
+    case FP8Q_BSCALE_BLOCK_T:
+      return f32 ? launch_mx<FP8Q_BSCALE_BLOCK_T, true, false>(ta, tb, a, tiles, s)
+                 : launch_mx<FP8Q_BSCALE_BLOCK_T, false, false>(ta, tb, a, tiles, s);
+    default:
+      return f32 ? launch_mx<FP8Q_BSCALE_ROW, true, false>(ta, tb, a, tiles, s)
+                 : launch_mx<FP8Q_BSCALE_ROW, false, false>(ta, tb, a, tiles, s);
+  }
+}
+
+fp8q_status mx_entry(const void *a, int64_t lda, const float *sa, int64_t ld_sa, const void *b,
+                     int64_t ldb, const float *sb, int64_t ld_sb, int bkind, void *c, int64_t ldc,
+                     int out_dtype, int64_t M, int64_t N, int64_t K, void *stream, bool accum) {
+  if (bkind != FP8Q_BSCALE_BLOCK && bkind != FP8Q_BSCALE_BLOCK_T && bkind != FP8Q_BSCALE_ROW)
+    return FP8Q_ERR_INVALID;
+  if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP32) return FP8Q_ERR_INVALID;
+  if (M < 0 || N < 0 || K < 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (M >= (1ll << 31) - kTileM || N >= (1ll << 31) - BN || K >= (1ll << 31)) return FP8Q_ERR_SHAPE;
+  if (ldc < N || ld_sa < M) return FP8Q_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8Q_OK;
+  if (!c) return FP8Q_ERR_INVALID;
+  const int64_t esz = out_dtype == FP8Q_OUT_FP32 ? 4 : 2;
+  if (!aligned16(c) || (ldc * esz) % 16) return FP8Q_ERR_ALIGN;
+  const int64_t KB = K / 128, NB = (N + 127) / 128;
+  auto st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  if (fp8q_status e = device_info(dev)) return e;
+  if (K == 0) {  // empty sum: C = 0 (or C unchanged when accumulating)
+    if (accum) return FP8Q_OK;
+    return cudaMemset2DAsync(c, static_cast<size_t>(ldc * esz), 0, static_cast<size_t>(N * esz),
+                             static_cast<size_t>(M), st) == cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
+  }
+  if (lda < K || ldb < K) return FP8Q_ERR_SHAPE;
+  if (!a || !b || !sa || !sb) return FP8Q_ERR_INVALID;
+  if (!aligned16(a) || !aligned16(b) || lda % 16 || ldb % 16 || !aligned4(sa) || !aligned4(sb))
+    return FP8Q_ERR_ALIGN;
+  if (bkind == FP8Q_BSCALE_BLOCK && ld_sb < KB) return FP8Q_ERR_SHAPE;
+  if (bkind == FP8Q_BSCALE_BLOCK_T && ld_sb < NB) return FP8Q_ERR_SHAPE;
+  if (bkind == FP8Q_BSCALE_ROW && ld_sb < N) return FP8Q_ERR_SHAPE;
+  if (dev.max_smem_optin < static_cast<int>(kSmemBytes)) return FP8Q_ERR_UNSUPPORTED;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K, lda, 128, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, K, ldb, 128, BN / 2,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return FP8Q_ERR_CUDA;
+  MxArgs args{};
+  args.sa = sa;
+  args.ld_sa = ld_sa;
+  args.sb = sb;
+  args.ld_sb = ld_sb;
+  args.c = c;
+  args.ldc = ldc;
+  args.M = static_cast<int>(M);
+  args.N = static_cast<int>(N);
+  args.num_kb = static_cast<int>(KB);
+  args.tiles_m = static_cast<int>((M + kTileM - 1) / kTileM);
+  args.tiles_n = static_cast<int>((N + BN - 1) / BN);
+  args.timeout_ns = wait_timeout_ns().load();
+  const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
+  if (tiles >= (1ll << 31)) return FP8Q_ERR_SHAPE;
+  return accum ? dispatch_mx<true>(bkind, true, ta, tb, args, tiles, st)
+               : dispatch_mx<false>(bkind, out_dtype == FP8Q_OUT_FP32, ta, tb, args, tiles, st);
+}
+
+}  // namespace
+
+fp8q_status mx_status_take(cudaStream_t s) {
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FP8Q_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mx_status, sizeof(int)) != cudaSuccess) return FP8Q_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_mx_status, &zero, sizeof(int)) != cudaSuccess) return FP8Q_ERR_CUDA;
+  }
+  return static_cast<fp8q_status>(v);
+}
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" fp8q_status fp8q_gemm_pow2(const void *a, int64_t lda, const float *sa, int64_t ld_sa,
+                                      const void *b, int64_t ldb, const float *sb, int64_t ld_sb,
+                                      int bscale_kind, void *c, int64_t ldc, int out_dtype,
+                                      int64_t M, int64_t N, int64_t K, void *stream) {
+  return mx_entry(a, lda, sa, ld_sa, b, ldb, sb, ld_sb, bscale_kind, c, ldc, out_dtype, M, N, K,
+                  stream, false);
+}
+
+extern "C" fp8q_status fp8q_gemm_pow2_accumulate(const void *a, int64_t lda, const float *sa,
+                                                 int64_t ld_sa, const void *b, int64_t ldb,
+                                                 const float *sb, int64_t ld_sb, int bscale_kind,
+                                                 float *c, int64_t ldc, int64_t M, int64_t N,
+                                                 int64_t K, void *stream) {
+  return mx_entry(a, lda, sa, ld_sa, b, ldb, sb, ld_sb, bscale_kind, c, ldc, FP8Q_OUT_FP32, M, N,
+                  K, stream, true);
+}

@@ -217,6 +217,38 @@ fp8q_status fp8q_gemm_accumulate(const void *a, int64_t lda, const float *sa,
                                  int64_t K, void *stream);
 
 /*
+ * fp8q_gemm for power-of-two scales, on the tensor cores' block-scaled MMA.
+ * The method allows scaling factors that are integral powers of two
+ * ([dssusan] paragraph 1) and recommends tensor cores that take the group
+ * scales themselves ([dssusan] paragraph 3); Blackwell's microscaling MMA
+ * ("Deepseek - Not For everyone", paragraph 3) multiplies each 32-wide K
+ * block of A and B by a power of two inside the MMA.  This call computes the
+ * same product as fp8q_gemm, with the K-group scales applied by the MMA and
+ * the sum over all K-groups accumulated in FP32 by the tensor cores (no
+ * per-group FP32 fold by the CUDA cores).
+ *   Arguments, layouts, alignment and return codes: as fp8q_gemm.
+ *   Precondition: every scale the product reads (sa of rows < M, sb of
+ *   columns < N, K-groups < K/128) is a power of two 2^e, -127 <= e <= 127 --
+ *   what the quantisers produce with FP8Q_SCALE_POW2.  Any other value is
+ *   used by its binary exponent alone, and the kernel records
+ *   FP8Q_ERR_INVALID in a device status word that fp8q_sync_status reports.
+ *   K == 0 writes zeros (fp8q_gemm_pow2) or leaves C unchanged (_accumulate).
+ * Tiles are 256 x 256 (a pair of CTAs per tile).
+ */
+fp8q_status fp8q_gemm_pow2(const void *a, int64_t lda, const float *sa,
+                           int64_t ld_sa, const void *b, int64_t ldb,
+                           const float *sb, int64_t ld_sb, int bscale_kind,
+                           void *c, int64_t ldc, int out_dtype, int64_t M,
+                           int64_t N, int64_t K, void *stream);
+
+/* C (FP32) += the fp8q_gemm_pow2 product; as fp8q_gemm_accumulate otherwise. */
+fp8q_status fp8q_gemm_pow2_accumulate(const void *a, int64_t lda, const float *sa,
+                                      int64_t ld_sa, const void *b, int64_t ldb,
+                                      const float *sb, int64_t ld_sb, int bscale_kind,
+                                      float *c, int64_t ldc, int64_t M, int64_t N,
+                                      int64_t K, void *stream);
+
+/*
  * Grouped FP8 GEMM for MoE experts: rows [offs[g], offs[g+1]) of A (tokens
  * sorted by expert, top-1 routing) are multiplied by expert g's weight.
  *   a     E4M3 [M][lda], sa at sa[kb * ld_sa + m] as in fp8q_gemm.
