@@ -14,26 +14,27 @@
 // product as the FP32-scale path's, accumulated over the whole K in the FP32
 // TMEM accumulator with no per-group fold by the CUDA cores.
 //
-// Roles (384 threads; CTA pairs, tile 256 x 256, one MMA thread per pair):
-//   warp 0      TMA producer: this CTA's 128 rows of A and 128 rows of B per
+// Roles (384 threads; CTA pairs, tile 256 x 224, one MMA thread per pair):
+//   warp 0      TMA producer: this CTA's 128 rows of A and 112 rows of B per
 //               K-group into a kStages ring, completing on the leading CTA's
 //               "full" barrier.
 //   warp 1      MMA issuer (leading CTA): per K-group 4 x tcgen05.mma
-//               .cta_group::2 .kind::mxf8f6f4 .block_scale (M=256, N=256,
-//               K=32) into one TMEM accumulator (columns 0-255), reading the
-//               scale exponents of the current scale stage.
+//               .cta_group::2 .kind::mxf8f6f4 .block_scale (M=256, N=224,
+//               K=32) into one of two TMEM accumulators (columns 0-223 and
+//               224-447, alternating by tile), reading the scale exponents of
+//               the current scale stage.
 //   warps 4-11  scale producers and epilogue.  Scale stage s (TMEM columns
-//               256 + 16 s .. +15, 16 stages) holds the exponents of four
+//               448 + 16 s .. +15, 4 stages) holds the exponents of four
 //               consecutive K-groups, one byte per group: warps 4-7 write the
 //               A exponents of their rows (column +q for lane quarter q),
-//               warps 8-11 the B exponents of the tile's 256 columns (columns
-//               +8..+15, the same in every lane quarter).  After the last
-//               K-group of a tile they read the accumulator (each thread 128
-//               columns of its row), release it, and store C.
+//               warps 8-11 the B exponents of the tile's 224 columns (columns
+//               +8..+14, the same in every lane quarter).  They drain a
+//               tile's accumulator (each thread 112 columns of its row) while
+//               the tensor cores fill the other one, and store C.
 //
-// The epilogue runs up to 16 scale stages (64 K-groups) ahead of the MMA
-// within a tile and into the next tile before draining the current one, so
-// the only pause of the tensor cores between tiles is the accumulator read.
+// 224-column tiles divide the model widths 7168 exactly and leave TMEM room
+// for two accumulators plus the scale ring, so the tensor cores never wait
+// for an accumulator to be read out.
 // A scale that is not a power of two (2^-127 .. 2^127) is a caller error: the
 // kernel uses its exponent and records FP8Q_ERR_INVALID in its status word.
 // Every wait is bounded in time (as in the FP32-scale GEMM).
@@ -55,11 +56,14 @@ __device__ int g_mx_status;
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int kAccBufs = 1;                     // TMEM accumulators (tiles in flight)
 constexpr int kTileM = 2 * BM;                  // C rows per pair tile
-constexpr int kStages = 6;                      // operand ring depth
 constexpr uint32_t kABytes = BM * BK;           // per CTA per stage
 constexpr uint32_t kBBytes = (BN / 2) * BK;     // per CTA per stage (half the columns)
 constexpr uint32_t kTxBytes = 2 * (kABytes + kBBytes);
+constexpr int kStages = 210 * 1024 / (kABytes + kBBytes) < 10
+                            ? static_cast<int>(210 * 1024 / (kABytes + kBBytes))
+                            : 10;               // operand ring depth
 constexpr size_t kRingBytes = static_cast<size_t>(kStages) * (kABytes + kBBytes);
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + kEpiWarps * 32;
@@ -67,14 +71,20 @@ constexpr int kLaunchRegs = 168;                // must match ptxas' count (chec
 constexpr int kCtlRegs = 40, kEpiRegs = 232;
 static_assert(kCtlRegs + 2 * kEpiRegs <= 3 * kLaunchRegs, "register split must fit the launch");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = BN;               // accumulator: columns [0, 256)
-constexpr int kSfStages = 16;                   // scale stages: columns [256, 512)
+constexpr uint32_t kAccCols = kAccBufs * BN;    // accumulators: columns [0, kAccCols)
+constexpr int kSfStages = (512 - kAccCols) / 16 < 16 ? (512 - kAccCols) / 16 : 16;
 constexpr uint32_t kSfStageCols = 16;
-constexpr uint32_t kSfbOffset = 8;              // B exponents at +8..+15 of a stage
+constexpr uint32_t kSfbOffset = 8;              // B exponents at +8..+14 of a stage
+constexpr int kBCols32 = BN / 32;               // 32-column groups of B per tile (7)
+constexpr int kEpiCols = BN / 2;                // columns each epilogue thread drains (112)
+static_assert(BN % 128 == 0 && kEpiCols % 16 == 0,
+              "tile width: whole 128-column scale blocks (and full-rate MMA widths)");
+// stages of the next tile written before the previous tile is drained: with
+// one accumulator the drain gates the next tile, so a short run-ahead keeps it
+// from waiting on the current tile's last stages
+constexpr int kRunAhead = kAccBufs == 1 ? 6 : kSfStages;
 static_assert(kAccCols + kSfStages * kSfStageCols <= kTmemCols, "TMEM budget");
 constexpr int kGroupsPerStage = 4;              // one byte per K-group in a 32-bit cell
-constexpr int kRunAhead = 6;                    // stages of the next tile written before a drain
-static_assert(kRunAhead < kSfStages, "run-ahead must not wait on the next tile's MMAs");
 constexpr int kGroupM = 16;                     // L2 rasterisation band (m-tiles)
 constexpr uint64_t kDrainNs = 1000000000ull;
 
@@ -96,8 +106,8 @@ struct alignas(8) MxCtl {
   uint64_t empty[kStages];
   uint64_t sfull[kSfStages];   // leading CTA: scale stage written (16 warp arrivals)
   uint64_t sempty[kSfStages];  // every CTA: scale stage consumed by the MMAs
-  uint64_t tfull;              // every CTA: accumulator complete
-  uint64_t tempty;             // leading CTA: accumulator read (16 warp arrivals)
+  uint64_t tfull[kAccBufs];    // every CTA: accumulator complete
+  uint64_t tempty[kAccBufs];   // leading CTA: accumulator read (16 warp arrivals)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -171,8 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->sfull[i]), 2 * kEpiWarps);
       mbar_init(smem_u32(&ctl->sempty[i]), 1);
     }
-    mbar_init(smem_u32(&ctl->tfull), 1);
-    mbar_init(smem_u32(&ctl->tempty), 2 * kEpiWarps);
+    for (int i = 0; i < kAccBufs; ++i) {
+      mbar_init(smem_u32(&ctl->tfull[i]), 1);
+      mbar_init(smem_u32(&ctl->tempty[i]), 2 * kEpiWarps);
+    }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -196,14 +208,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 4;
     const int q = warp & 3;          // lane quarter this warp may access
     const bool a_side = ew < 4;      // warps 4-7: A exponents; 8-11: B exponents
-    const int col_half = ew >> 2;    // epilogue: columns [128 * col_half, +128)
+    const int col_half = ew >> 2;    // epilogue: columns [kEpiCols * col_half, +kEpiCols)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
     const uint32_t sfull0 = mapa_shared(smem_u32(&ctl->sfull[0]), 0);
-    const uint32_t tempty0 = mapa_shared(smem_u32(&ctl->tempty), 0);
+    const uint32_t tempty0 = mapa_shared(smem_u32(&ctl->tempty[0]), 0);
     int ss = 0;           // next scale stage slot to write
     uint32_t sphase = 0;  // its phase
-    uint32_t tphase = 0;
+    uint32_t tphase = 0;  // bit b: phase of tfull[b]
     bool ok = true;
 
     // Scale production walks a cursor over (tile, stage) in the order the MMA
@@ -213,8 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stage, so loading them at use would put that latency on the critical path.
     //   A warps: raw[0..3] = sa of this thread's row, K-groups 4 js .. 4 js + 3.
     //   B warps, per-column scales: raw[4 c + j] = sb of column n0 + 32 c + lane.
-    //   B warps, block scales: raw[4 h + j] = the scale of 128-column block h.
-    constexpr int kRaw = kBScale == FP8Q_BSCALE_ROW ? 32 : 8;
+    //   B warps, block scales: raw[4 h + j] = the scale of 128-column block h
+    //   of the tile (column group c lies in block c / 4).
+    constexpr int kRaw = kBScale == FP8Q_BSCALE_ROW ? kBCols32 * kGroupsPerStage
+                                                    : (BN / 128) * kGroupsPerStage;
     const int NB = (p.N + 127) / 128;
     auto load_raw = [&](int t, int js, float (&r)[kRaw]) {
       const MxTile tl = mx_tile_of(t, p);
@@ -229,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             r[j] = __ldg(p.sa + static_cast<int64_t>(kb0 + j) * p.ld_sa + m);
       } else if (kBScale == FP8Q_BSCALE_ROW) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kBCols32; ++c) {
           const int n = tl.n0 + 32 * c + lane;
 #pragma unroll
           for (int j = 0; j < kGroupsPerStage; ++j)
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // columns past N in a partial block read zero-filled B rows, so the
         // block's own scale is as good as any for them
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < BN / 128; ++h) {
           const int nb = tl.n0 / 128 + h;
 #pragma unroll
           for (int j = 0; j < kGroupsPerStage; ++j)
@@ -279,10 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const int base = kBScale == FP8Q_BSCALE_ROW ? 4 * c : 4 * (c / 4);
-          uint32_t word = 0;
+          uint32_t word = 0x7F7F7F7Fu;  // column group past the tile: unused, 2^0
+          if (c < kBCols32) {
+            const int base = kBScale == FP8Q_BSCALE_ROW ? 4 * c : 4 * (c / 4);
+            word = 0;
 #pragma unroll
-          for (int j = 0; j < kGroupsPerStage; ++j) word |= ue8m0_of(raw[base + j], bad) << (8 * j);
+            for (int j = 0; j < kGroupsPerStage; ++j) word |= ue8m0_of(raw[base + j], bad) << (8 * j);
+          }
           w[c] = word;
         }
         tmem_st_32x32b_x8(tmem_base + lane_addr + col + kSfbOffset, w);
@@ -303,51 +320,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
-      const MxTile tl = mx_tile_of(t, p);
-      while (ok && cur_t == t) ok = produce();  // the rest of this tile's stages
-      // run ahead into the next tile, enough stages to cover the drain and the
-      // stores below.  Stage js of the next tile reuses the slot of this
-      // tile's stage js + nst - kSfStages, so a short run-ahead finishes well
-      // before this tile's last MMAs and never delays the drain; it must also
-      // stay under kSfStages, or a wait would depend on the next tile's own
-      // MMAs (which need the drain).
-      const int lim = nst < kRunAhead ? nst : kRunAhead;
-      while (ok && cur_t == t + tile_step && cur_t < total_tiles && cur_js < lim) ok = produce();
-      if (!ok) break;
-
-      // ---- drain the accumulator: this thread's row, 128 columns
-      const bool got = mbar_wait_bounded(smem_u32(&ctl->tfull), tphase, abort_flag,
-                                         &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tphase ^= 1;
+    // Read tile t's accumulator (buffer buf), release it, store C.
+    auto drain = [&](int t, int buf) -> bool {
+      const bool got = mbar_wait_bounded(smem_u32(&ctl->tfull[buf]), (tphase >> buf) & 1u,
+                                         abort_flag, &g_mx_status, p.timeout_ns,
+                                         FP8Q_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      tphase ^= 1u << buf;
       tc_fence_after();
-      uint32_t v[8][16];
-      const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(col_half * 128);
+      constexpr int kChunks = kEpiCols / 16;
+      uint32_t v[kChunks][16];
+      const uint32_t taddr = tmem_base + lane_addr +
+                             static_cast<uint32_t>(buf * BN + col_half * kEpiCols);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int i = 0; i < kChunks; ++i) tmem_ld_32x32b_x16(taddr + i * 16, v[i]);
+      tmem_wait_ld_tied(v[0]);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) tmem_ld_32x32b_x16(taddr + (4 * h + b) * 16, v[4 * h + b]);
-        tmem_wait_ld_tied(v[4 * h]);
-#pragma unroll
-        for (int b = 1; b < 4; ++b) reg_tie(v[4 * h + b]);
-      }
+      for (int i = 1; i < kChunks; ++i) reg_tie(v[i]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0);
+      if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf) * 8u);
 
-      // ---- store C
+      const MxTile tl = mx_tile_of(t, p);
       const int m = tl.m0 + row_in_tile;
-      const int ncol0 = tl.n0 + col_half * 128;
+      const int ncol0 = tl.n0 + col_half * kEpiCols;
       if (m < p.M && ncol0 < p.N) {
-        const bool full = ncol0 + 128 <= p.N;
+        const bool full = ncol0 + kEpiCols <= p.N;
         if (kOutF32) {
           float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
-          for (int j = 0; j < 128; j += 4) {
+          for (int j = 0; j < kEpiCols; j += 4) {
             float x[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(v[(j + e) / 16][(j + e) % 16]);
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nv_bfloat16 *crow =
               static_cast<__nv_bfloat16 *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
-          for (int j = 0; j < 128; j += 8) {
+          for (int j = 0; j < kEpiCols; j += 8) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -389,7 +391,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      return true;
+    };
+
+    // Tile t's accumulator is read at the top of the next iteration, while the
+    // tensor cores fill the other buffer with tile t + step; the scale stages
+    // of the next tile are written ahead (up to kSfStages of them: stage js of
+    // the next tile reuses the slot of this tile's stage nst + js - kSfStages,
+    // so no wait depends on the next tile's own MMAs).
+    int prev_t = -1, prev_buf = 0;
+    int i = 0;
+    for (int t = tile_first; ok && t < total_tiles; t += tile_step, ++i) {
+      if (prev_t >= 0 && !(ok = drain(prev_t, prev_buf))) break;
+      while (ok && cur_t == t) ok = produce();  // the rest of this tile's stages
+      const int lim = nst < kRunAhead ? nst : kRunAhead;
+      while (ok && cur_t == t + tile_step && cur_t < total_tiles && cur_js < lim) ok = produce();
+      prev_t = t;
+      prev_buf = i % kAccBufs;
     }
+    if (ok && prev_t >= 0) ok = drain(prev_t, prev_buf);
     __syncwarp();
     tc_fence_before();
     cluster_sync_all();
@@ -442,17 +462,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int ss = 0;
       uint32_t sphase = 0;
-      uint32_t tphase = 0;
+      uint32_t tphase = 0;  // bit b: phase of tempty[b]
       bool ok = true, issued = false;
-      for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
-        // the accumulator must have been read out (both CTAs)
-        if (!mbar_wait_bounded(smem_u32(&ctl->tempty), tphase ^ 1, abort_flag, &g_mx_status,
-                               p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
+      int i = 0;
+      for (int t = tile_first; ok && t < total_tiles; t += tile_step, ++i) {
+        // this tile's accumulator must have been read out (both CTAs)
+        const int buf = i % kAccBufs;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[buf]), ((tphase >> buf) & 1u) ^ 1u,
+                               abort_flag, &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
           ok = false;
           break;
         }
-        tphase ^= 1;
+        tphase ^= 1u << buf;
         tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           const uint32_t j = static_cast<uint32_t>(kb % kGroupsPerStage);
           if (j == 0) {
@@ -474,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t idesc = idesc_mx_e4m3(kTileM, BN, j, j);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            mma_mx_pair(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, sfa, sfa + kSfbOffset,
+            mma_mx_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, sfa, sfa + kSfbOffset,
                         (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair_multicast(smem_u32(&ctl->empty[stage]), 0x3);
           if (j == kGroupsPerStage - 1 || kb == p.num_kb - 1) {
@@ -491,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit_pair_multicast(smem_u32(&ctl->tfull), 0x3);
+        mma_commit_pair_multicast(smem_u32(&ctl->tfull[buf]), 0x3);
       }
       if (!ok && issued) {
         mma_commit_pair_multicast(smem_u32(&ctl->drain), 0x1);
