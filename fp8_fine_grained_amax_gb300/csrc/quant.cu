@@ -140,31 +140,52 @@ constexpr int kTileThreads = 512;
 
 // ------------------------------------------------------------------ 128x1
 // Persistent: each CTA walks 128-token x 128-channel tiles (channel blocks
-// fastest) with a two-deep shared-memory ring filled by TMA, so the next tile
-// streams in while this one is reduced and converted.  Per tile:
-//  - optionally the 1x128 codes of each row (half-warp per row, shuffles),
-//  - each channel's max-abs over the 128 tokens, its scale,
-//  - each channel's 128 codes written contiguously (transposed output).
-// Rows past C are zero-filled by TMA and never stored.
+// fastest) with a two-deep ring of input tiles filled by TMA, so the next
+// tile streams in while this one is reduced and converted.
+//  - Input: two 64-channel halves per tile, 128-byte swizzled (the 16-byte
+//    chunk k of token row r sits at chunk k ^ (r % 8)), so that ldmatrix.trans
+//    reads 8 consecutive token rows of one chunk without bank conflicts.
+//  - Warp w owns channels 8w .. 8w+7: four ldmatrix.x4.trans give each thread
+//    32 values of one channel (c = 8w + lane/4; tokens 8m + 2(lane%4) + {0,1},
+//    m = 0..15).  The channel's max-abs is a packed max over them and two
+//    shuffles; no other warp is involved.
+//  - Codes go to a swizzled shared-memory copy of the transposed tile
+//    (channel rows of 128 bytes) that one TMA store writes out, so the
+//    transposed output costs no per-thread global stores.
+//  - Optionally the 1x128 codes of each token row (half-warp per row).
+// Channels past C are zero-filled by TMA and clipped by the TMA store.
 constexpr uint32_t kTileBytesBF16 = 128 * 128 * 2;
+constexpr uint32_t kHalfBytesBF16 = kTileBytesBF16 / 2;   // 128 tokens x 64 channels
+constexpr uint32_t kTileBytesQ = 128 * 128;                // 128 channels x 128 tokens
+
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
 
 template <bool kPow2, bool kRows>
 __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
-    const __grid_constant__ CUtensorMap tmX, int64_t T, int64_t C, uint8_t *__restrict__ qT,
-    int64_t ldqT, float *__restrict__ sT, int64_t ld_sT, uint8_t *__restrict__ q_rows,
+    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmQ, int64_t T,
+    int64_t C, float *__restrict__ sT, int64_t ld_sT, uint8_t *__restrict__ q_rows,
     int64_t ldq_rows, float *__restrict__ s_rows, int64_t ld_s_rows, uint64_t timeout_ns) {
   extern __shared__ uint8_t dsm_raw[];
-  auto tiles = reinterpret_cast<uint32_t(*)[128][64]>(
+  uint8_t *base = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ float red[8][128];
-  __shared__ float col_inv[128];
+  const uint32_t in0 = smem_u32(base);                    // 2 x 32 KB input tiles
+  const uint32_t st0 = in0 + 2 * kTileBytesBF16;          // 2 x 16 KB staged codes
   __shared__ uint64_t full[2];
   __shared__ int abort_flag;
 
-  const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t ncb = (C + 127) / 128;
   const int64_t ntiles = ncb * (T / 128);
   int pending[2] = {-1, -1};  // thread 0: parity of the copy in flight per buffer
+  auto issue_load = [&](int b, int64_t t) {
+    const uint32_t bar = smem_u32(&full[b]);
+    mbar_arrive_expect_tx(bar, kTileBytesBF16);
+    const int32_t c0 = static_cast<int32_t>((t % ncb) * 128), t0 = static_cast<int32_t>((t / ncb) * 128);
+    tma_load_2d(in0 + b * kTileBytesBF16, &tmX, bar, c0, t0);
+    tma_load_2d(in0 + b * kTileBytesBF16 + kHalfBytesBF16, &tmX, bar, c0 + 64, t0);
+  };
   if (tid == 0) {
     mbar_init(smem_u32(&full[0]), 1);
     mbar_init(smem_u32(&full[1]), 1);
@@ -173,35 +194,42 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
     for (int b = 0; b < 2; ++b) {
       const int64_t t = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
       if (t < ntiles) {
-        mbar_arrive_expect_tx(smem_u32(&full[b]), kTileBytesBF16);
-        tma_load_2d(smem_u32(&tiles[b][0][0]), &tmX, smem_u32(&full[b]),
-                    static_cast<int32_t>((t % ncb) * 128), static_cast<int32_t>((t / ncb) * 128));
+        issue_load(b, t);
         pending[b] = 0;
       }
     }
   }
   __syncthreads();
 
+  // this warp's channels: half h, 16-byte chunk j of each token row
+  const uint32_t h = static_cast<uint32_t>(warp >> 3), j = static_cast<uint32_t>(warp & 7);
+  const int cw = 8 * warp + (lane >> 2);  // this thread's channel within the tile
   int it = 0;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int buf = it & 1;
     const bool got = mbar_wait_bounded(smem_u32(&full[buf]), (it >> 1) & 1, &abort_flag,
                                        &g_quant_status, timeout_ns, FP8Q_ERR_TIMEOUT);
     if (__syncthreads_or(!got)) {
-      if (tid == 0)  // let this CTA's own copies land before it exits
+      if (tid == 0) {  // let this CTA's own copies land before it exits
         for (int b = 0; b < 2; ++b)
           if (pending[b] >= 0) mbar_wait_drain(smem_u32(&full[b]), pending[b]);
+        bulk_wait_group_all();
+      }
       return;
     }
     if (tid == 0) pending[buf] = -1;
-    uint32_t(*tile)[64] = tiles[buf];
+    const uint32_t tin = in0 + buf * kTileBytesBF16;
     const int64_t c0 = (t % ncb) * 128, t0 = (t / ncb) * 128;
 
     if (kRows) {  // C % 128 == 0 here: every chunk is in range
+      const int hw = tid >> 4, l16 = tid & 15;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int r = hw + 32 * i;
-        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][l16 * 4]);
+        const uint32_t r = static_cast<uint32_t>(hw + 32 * i);
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(tin + (l16 >> 3) * kHalfBytesBF16 + swz128(r, l16 & 7)));
         uint32_t mb = absmax_bits8(v);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
@@ -212,58 +240,54 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
       }
     }
 
-    const int cp = tid & 63, tq = tid >> 6;
+    // ---- 128x1: this thread's channel, 32 of its 128 tokens
+    uint32_t v[16];
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      uint32_t r4[4];
+      ldmatrix_x4_trans(tin + h * kHalfBytesBF16 + swz128(32u * qd + lane, j), r4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[4 * qd + e] = r4[e];
+    }
     uint32_t mw = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) mw = umax16x2(mw, tile[tq * 16 + j][cp] & 0x7FFF7FFFu);
-    red[tq][2 * cp] = __uint_as_float(mw << 16);
-    red[tq][2 * cp + 1] = __uint_as_float(mw & 0xFFFF0000u);
-    __syncthreads();
-    if (tid < 128) {
-      float amax = red[0][tid];
+    for (int m = 0; m < 16; ++m) mw = umax16x2(mw, v[m] & 0x7FFF7FFFu);
+    mw = umax16x2(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
+    mw = umax16x2(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
+    float sc, inv;
+    group_scale(bits_to_f32_max(mw), kPow2, sc, inv);
+    if ((lane & 3) == 0 && c0 + cw < C) sT[(t0 / 128) * ld_sT + c0 + cw] = sc;
+    uint32_t code[16];  // tokens 8m + 2(lane%4), +1 of channel cw
 #pragma unroll
-      for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i][tid]);
-      float sc, inv;
-      group_scale(amax, kPow2, sc, inv);
-      col_inv[tid] = inv;
-      if (c0 + tid < C) sT[(t0 / 128) * ld_sT + c0 + tid] = sc;
-    }
-    __syncthreads();
+    for (int m = 0; m < 16; ++m)
+      code[m] = pack_e4m3x2(__fmul_rn(bf16_lo(v[m]), inv), __fmul_rn(bf16_hi(v[m]), inv));
 
-    // transposed codes: thread (cc, tq4) owns channel c0 + cc and tokens
-    // 32 tq4 .. 32 tq4 + 31, i.e. one full 32-byte sector of that channel's row
-    const int cc = tid & 127, tq4 = tid >> 7;
-    const int64_t c = c0 + cc;
-    if (c < C) {
-      const float inv = col_inv[cc];
-      const int word = cc >> 1, shift = (cc & 1) ? 0 : 16;  // BF16 of channel cc in the word
-      uint32_t out[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float f[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          f[e] = __fmul_rn(
-              __uint_as_float((tile[tq4 * 32 + 4 * j + e][word] << shift) & 0xFFFF0000u), inv);
-        out[j] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
-      }
-      uint4 *dst = reinterpret_cast<uint4 *>(qT + c * ldqT + t0 + tq4 * 32);
-      dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-      dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
-    }
-    __syncthreads();  // every thread is done with this buffer and col_inv
+    // the staged codes written two tiles ago must have been read by their store
+    if (tid == 0) bulk_wait_group_read<1>();
+    __syncthreads();  // every thread is done with input buffer `buf` and may reuse stage `buf`
     if (tid == 0) {
       const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
       if (tn < ntiles) {
         // generic-proxy reads of the buffer above, async-proxy write below
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(smem_u32(&full[buf]), kTileBytesBF16);
-        tma_load_2d(smem_u32(&tile[0][0]), &tmX, smem_u32(&full[buf]),
-                    static_cast<int32_t>((tn % ncb) * 128), static_cast<int32_t>((tn / ncb) * 128));
+        fence_proxy_async_shared();
+        issue_load(buf, tn);
         pending[buf] = ((it + 2) >> 1) & 1;
       }
     }
+    const uint32_t stg = st0 + buf * kTileBytesQ;
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+      st_shared_u16(stg + swz128(static_cast<uint32_t>(cw), static_cast<uint32_t>(m >> 1)) +
+                        8u * (m & 1) + 2u * (lane & 3),
+                    code[m]);
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_2d(&tmQ, stg, static_cast<int32_t>(t0), static_cast<int32_t>(c0));
+      bulk_commit_group();
+    }
   }
+  if (tid == 0) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ 128x1 from FP8
@@ -506,12 +530,12 @@ __global__ void __launch_bounds__(256) cast_e4m3_kernel(const float *__restrict_
 
 bool valid_mode(int m) { return m == FP8Q_SCALE_FP32 || m == FP8Q_SCALE_POW2; }
 
-constexpr int kActTCtasPerSm = 3;  // 2 x 32 KB ring + 6 KB each: three fit per SM
-constexpr size_t kActTSmem = 2 * kTileBytesBF16 + 1024;
+constexpr int kActTCtasPerSm = 2;  // 2 x 32 KB input ring + 2 x 16 KB staged codes each
+constexpr size_t kActTSmem = 2 * kTileBytesBF16 + 2 * kTileBytesQ + 1024;
 
 template <bool kPow2, bool kRows>
-fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX, int64_t T,
-                         int64_t C, uint8_t *qT, int64_t ldqT, float *sT, int64_t ld_sT,
+fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX,
+                         const CUtensorMap &tmQ, int64_t T, int64_t C, float *sT, int64_t ld_sT,
                          uint8_t *q_rows, int64_t ldq_rows, float *s_rows, int64_t ld_s_rows,
                          uint64_t timeout_ns) {
   auto kern = quant_act_T_kernel<kPow2, kRows>;
@@ -528,8 +552,8 @@ fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX, 
       attr_set[dev] = true;
     }
   }
-  kern<<<grid, kTileThreads, kActTSmem, s>>>(tmX, T, C, qT, ldqT, sT, ld_sT, q_rows, ldq_rows,
-                                             s_rows, ld_s_rows, timeout_ns);
+  kern<<<grid, kTileThreads, kActTSmem, s>>>(tmX, tmQ, T, C, sT, ld_sT, q_rows, ldq_rows, s_rows,
+                                             ld_s_rows, timeout_ns);
   return launch_status();
 }
 
@@ -579,31 +603,35 @@ extern "C" fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int
   if (rows && (!aligned16(q_rows) || !aligned4(s_rows) || ldq_rows % 16)) return FP8Q_ERR_ALIGN;
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  CUtensorMap tmX;
+  // input: 64-channel x 128-token boxes, 128-byte swizzle; output: the
+  // transposed codes qT [C][T], 128-token x 128-channel boxes, same swizzle
+  CUtensorMap tmX, tmQ;
   if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(T),
-                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldx) * 2, 128, 128,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
+                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldx) * 2, 64, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, qT, static_cast<uint64_t>(C),
+                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return FP8Q_ERR_CUDA;
   const int64_t ntiles = ((C + 127) / 128) * (T / 128);
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * kActTCtasPerSm;
   const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
   auto s = static_cast<cudaStream_t>(stream);
-  auto qp = static_cast<uint8_t *>(qT);
   auto rp = static_cast<uint8_t *>(q_rows);
   const uint64_t tmo = wait_timeout_ns().load();
   const bool p2 = scale_mode == FP8Q_SCALE_POW2;
   fp8q_status st = FP8Q_OK;
   if (p2 && rows)
-    st = launch_act_T<true, true>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+    st = launch_act_T<true, true>(grid, s, tmX, tmQ, T, C, sT, ld_sT, rp, ldq_rows, s_rows,
                                   ld_s_rows, tmo);
   else if (p2)
-    st = launch_act_T<true, false>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+    st = launch_act_T<true, false>(grid, s, tmX, tmQ, T, C, sT, ld_sT, rp, ldq_rows, s_rows,
                                    ld_s_rows, tmo);
   else if (rows)
-    st = launch_act_T<false, true>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+    st = launch_act_T<false, true>(grid, s, tmX, tmQ, T, C, sT, ld_sT, rp, ldq_rows, s_rows,
                                    ld_s_rows, tmo);
   else
-    st = launch_act_T<false, false>(grid, s, tmX, T, C, qp, ldqT, sT, ld_sT, rp, ldq_rows, s_rows,
+    st = launch_act_T<false, false>(grid, s, tmX, tmQ, T, C, sT, ld_sT, rp, ldq_rows, s_rows,
                                     ld_s_rows, tmo);
   return st;
 }
