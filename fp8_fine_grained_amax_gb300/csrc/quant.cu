@@ -374,20 +374,26 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
 
 // ------------------------------------------------------------------ 128x128
 // Grid (K / 128, ceil(N / 128)).  A CTA owns one block: reduces the block
-// max-abs (packed max, warp shuffles, then across the 16 warps), writes the
-// codes row-wise from registers and, if asked, transposed through shared
-// memory.
+// max-abs (packed max, warp shuffles, then across the 16 warps) and writes the
+// codes row-wise from registers.  With the transposed copy, the block also
+// goes to shared memory in two 128-byte-swizzled halves (as the 128x1
+// quantiser's TMA tiles); warp w reads columns 8w .. 8w+7 of all 128 rows
+// with ldmatrix.trans, and the transposed codes are staged and written by one
+// TMA store (rows past N clipped by it).
 template <bool kPow2, bool kTrans>
 __global__ void __launch_bounds__(kTileThreads) quant_weight_kernel(
     const uint16_t *__restrict__ w, int64_t N, int64_t ldw, uint8_t *__restrict__ q, int64_t ldq,
-    uint8_t *__restrict__ qT, int64_t ldqT, float *__restrict__ sb, int64_t ld_sb) {
-  __shared__ uint32_t tile[kTrans ? 128 : 1][64];
+    const __grid_constant__ CUtensorMap tmQT, uint8_t *__restrict__ qT_ptr, int64_t ldqT,
+    float *__restrict__ sb, int64_t ld_sb) {
+  extern __shared__ uint8_t dsm_raw[];
   __shared__ uint32_t warp_amax[16];
   __shared__ float blk_inv;
 
   const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
   const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int64_t n0 = static_cast<int64_t>(blockIdx.y) * 128;
+  const uint32_t tin = kTrans ? ((smem_u32(dsm_raw) + 1023u) & ~1023u) : 0u;  // 2 x 16 KB
+  const uint32_t stg = tin + kTileBytesBF16;                                  // 16 KB
 
   uint4 v[4];
 #pragma unroll
@@ -403,7 +409,12 @@ __global__ void __launch_bounds__(kTileThreads) quant_weight_kernel(
   if ((tid & 31) == 0) warp_amax[tid >> 5] = mb;
   if (kTrans) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4 *>(&tile[hw + 32 * i][l16 * 4]) = v[i];
+    for (int i = 0; i < 4; ++i)
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                       tin + (l16 >> 3) * kHalfBytesBF16 +
+                       swz128(static_cast<uint32_t>(hw + 32 * i), static_cast<uint32_t>(l16 & 7))),
+                   "r"(v[i].x), "r"(v[i].y), "r"(v[i].z), "r"(v[i].w)
+                   : "memory");
   }
   __syncthreads();
   if (tid == 0) {
@@ -423,28 +434,52 @@ __global__ void __launch_bounds__(kTileThreads) quant_weight_kernel(
     if (n < N) *reinterpret_cast<uint2 *>(q + n * ldq + k0 + l16 * 8) = quantise8(v[i], inv);
   }
   if (kTrans) {
-    // thread (kk, nq4): column k0 + kk, rows n0 + 32 nq4 .. + 31, i.e. one full
-    // 32-byte sector of row k0 + kk of the transposed codes
-    const int kk = tid & 127, nq4 = tid >> 7;
-    const int word = kk >> 1, shift = (kk & 1) ? 0 : 16;
-    uint32_t out[8];
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t h = static_cast<uint32_t>(warp >> 3), j = static_cast<uint32_t>(warp & 7);
+    const uint32_t kw = static_cast<uint32_t>(8 * warp + (lane >> 2));  // this thread's column
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float f[4];
+    for (int qd = 0; qd < 4; ++qd) {
+      uint32_t r4[4];
+      ldmatrix_x4_trans(tin + h * kHalfBytesBF16 + swz128(32u * qd + lane, j), r4);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        f[e] = __fmul_rn(__uint_as_float((tile[nq4 * 32 + 4 * j + e][word] << shift) & 0xFFFF0000u),
-                         inv);
-      out[j] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+      for (int e = 0; e < 4; ++e) {
+        const int m = 4 * qd + e;  // rows 8m + 2(lane%4), +1
+        st_shared_u16(stg + swz128(kw, static_cast<uint32_t>(m >> 1)) + 8u * (m & 1) +
+                          2u * (lane & 3),
+                      pack_e4m3x2(__fmul_rn(bf16_lo(r4[e]), inv), __fmul_rn(bf16_hi(r4[e]), inv)));
+      }
     }
-    const int64_t nb0 = n0 + nq4 * 32;
-    uint8_t *row = qT + (k0 + kk) * ldqT + nb0;
-    if (nb0 + 32 <= N) {
-      reinterpret_cast<uint4 *>(row)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-      reinterpret_cast<uint4 *>(row)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    if (n0 + 128 <= N) {  // a whole block: one TMA store
+      fence_proxy_async_shared();
+      __syncthreads();
+      if (tid == 0) {
+        tma_store_2d(&tmQT, stg, static_cast<int32_t>(n0), static_cast<int32_t>(k0));
+        bulk_commit_group();
+        bulk_wait_group_all();
+      }
     } else {
-      for (int j = 0; j < 32 && nb0 + j < N; ++j)
-        row[j] = static_cast<uint8_t>(out[j >> 2] >> (8 * (j & 3)));
+      // the last, partial block: the TMA store would clip the row at 16-byte
+      // granularity and could write past N, so copy the staged rows out with
+      // bounds (thread: row kk, 32 bytes)
+      __syncthreads();
+      const uint32_t kk = static_cast<uint32_t>(tid >> 2);
+      uint8_t *row = qT_ptr + (k0 + kk) * ldqT + n0;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t chunk = 2u * (tid & 3) + c;
+        uint4 b;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                     : "r"(stg + swz128(kk, chunk)));
+        const int64_t nb = n0 + 16 * chunk;
+        if (nb + 16 <= N) {
+          *reinterpret_cast<uint4 *>(row + 16 * chunk) = b;
+        } else {
+          const uint32_t wds[4] = {b.x, b.y, b.z, b.w};
+          for (int e = 0; e < 16 && nb + e < N; ++e)
+            row[16 * chunk + e] = static_cast<uint8_t>(wds[e >> 2] >> (8 * (e & 3)));
+        }
+      }
     }
   }
 }
@@ -557,6 +592,31 @@ fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX,
   return launch_status();
 }
 
+constexpr size_t kWeightTSmem = kTileBytesBF16 + kTileBytesQ + 1024;  // transposed path only
+
+template <bool kPow2, bool kTrans>
+fp8q_status launch_weight(dim3 grid, cudaStream_t s, const uint16_t *w, int64_t N, int64_t ldw,
+                          uint8_t *q, int64_t ldq, const CUtensorMap &tmQT, uint8_t *qT,
+                          int64_t ldqT, float *sb, int64_t ld_sb) {
+  auto kern = quant_weight_kernel<kPow2, kTrans>;
+  const size_t smem = kTrans ? kWeightTSmem : 0;
+  if (kTrans) {
+    static bool attr_set[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+  }
+  kern<<<grid, kTileThreads, smem, s>>>(w, N, ldw, q, ldq, tmQT, qT, ldqT, sb, ld_sb);
+  return launch_status();
+}
+
 }  // namespace
 }  // namespace fp8q
 
@@ -656,18 +716,17 @@ extern "C" fp8q_status fp8q_quant_weight(const void *w, int64_t N, int64_t K, in
   auto s = static_cast<cudaStream_t>(stream);
   auto wp = static_cast<const uint16_t *>(w);
   auto qp = static_cast<uint8_t *>(q);
-  auto tp = static_cast<uint8_t *>(qT);
+  // the transposed codes qT [K][N]: 128-row x 128-column boxes, 128-byte swizzle
+  CUtensorMap tmQT{};
+  if (trans && !make_tmap_2d(&tmQT, CU_TENSOR_MAP_DATA_TYPE_UINT8, qT, static_cast<uint64_t>(K),
+                             static_cast<uint64_t>(N), static_cast<uint64_t>(ldqT), 128, 128,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+    return FP8Q_ERR_CUDA;
   const bool p2 = scale_mode == FP8Q_SCALE_POW2;
-  if (p2 && trans)
-    quant_weight_kernel<true, true><<<grid, kTileThreads, 0, s>>>(wp, N, ldw, qp, ldq, tp, ldqT, sb, ld_sb);
-  else if (p2)
-    quant_weight_kernel<true, false><<<grid, kTileThreads, 0, s>>>(wp, N, ldw, qp, ldq, tp, ldqT, sb, ld_sb);
-  else if (trans)
-    quant_weight_kernel<false, true><<<grid, kTileThreads, 0, s>>>(wp, N, ldw, qp, ldq, tp, ldqT, sb, ld_sb);
-  else
-    quant_weight_kernel<false, false>
-        <<<grid, kTileThreads, 0, s>>>(wp, N, ldw, qp, ldq, tp, ldqT, sb, ld_sb);
-  return launch_status();
+  if (p2 && trans) return launch_weight<true, true>(grid, s, wp, N, ldw, qp, ldq, tmQT, static_cast<uint8_t *>(qT), ldqT, sb, ld_sb);
+  if (p2) return launch_weight<true, false>(grid, s, wp, N, ldw, qp, ldq, tmQT, static_cast<uint8_t *>(qT), ldqT, sb, ld_sb);
+  if (trans) return launch_weight<false, true>(grid, s, wp, N, ldw, qp, ldq, tmQT, static_cast<uint8_t *>(qT), ldqT, sb, ld_sb);
+  return launch_weight<false, false>(grid, s, wp, N, ldw, qp, ldq, tmQT, static_cast<uint8_t *>(qT), ldqT, sb, ld_sb);
 }
 
 extern "C" fp8q_status fp8q_cast_e4m3(const float *x, int64_t n, void *q, void *stream) {
