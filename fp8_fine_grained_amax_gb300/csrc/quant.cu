@@ -291,85 +291,147 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 }
 
 // ------------------------------------------------------------------ 128x1 from FP8
-// Grid (C / 128, T / 128).  Requantises FP8-cached activations: input E4M3
-// [T][C] with one 1x128 scale per (token, 128 channels), output the 128x1
-// codes transposed.  Each value is first dequantised with one FP32 multiply,
-// x = fl32(decode(q) * s_row), exactly as a BF16 input would be read; the
-// codes are decoded exactly (E4M3 is a subset of FP16) into shared memory.
+// Persistent, like the BF16 128x1 quantiser.  Requantises FP8-cached
+// activations: input E4M3 [T][C] with one 1x128 scale per (token, 128
+// channels), output the 128x1 codes transposed.  Each value is first
+// dequantised with one FP32 multiply, x = fl32(decode(q) * s_row), exactly as a
+// BF16 input would be read.  Per tile: the raw codes arrive by TMA (two-deep
+// ring); they are decoded exactly (E4M3 is a subset of FP16) into a
+// 128-byte-swizzled FP16 tile; ldmatrix.trans reads it by channel; the
+// transposed codes leave through one TMA store.  The next tile's row scales
+// are loaded while this one is processed.
+constexpr uint32_t kTileBytesQ8 = 128 * 128;  // one tile of E4M3 codes
+
 template <bool kPow2>
 __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
-    const uint8_t *__restrict__ q, int64_t ldq, const float *__restrict__ s_rows,
-    int64_t ld_s_rows, uint8_t *__restrict__ qT, int64_t ldqT, float *__restrict__ sT,
-    int64_t ld_sT) {
-  __shared__ uint32_t tile[128][64];  // [token][channel pair], FP16x2 of the decoded codes
-  __shared__ float srow[128];
-  __shared__ float red[8][128];
-  __shared__ float col_inv[128];
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQT, int64_t T,
+    int64_t C, const float *__restrict__ s_rows, int64_t ld_s_rows, float *__restrict__ sT,
+    int64_t ld_sT, uint64_t timeout_ns) {
+  extern __shared__ uint8_t dsm_raw[];
+  __shared__ __align__(16) float srow[128];
+  __shared__ uint64_t full[2];
+  __shared__ int abort_flag;
+  const uint32_t raw0 = (smem_u32(dsm_raw) + 1023u) & ~1023u;  // 2 x 16 KB raw codes
+  const uint32_t tin = raw0 + 2 * kTileBytesQ8;                // 2 x 16 KB FP16 halves
+  const uint32_t st0 = tin + kTileBytesBF16;                   // 2 x 16 KB staged codes
 
   const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * 128;
-  if (tid < 128) srow[tid] = s_rows[blockIdx.x * ld_s_rows + t0 + tid];
-  uint2 raw[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint8_t *src = q + (t0 + hw + 32 * i) * ldq + c0 + l16 * 8;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-                 : "=r"(raw[i].x), "=r"(raw[i].y)
-                 : "l"(src));
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 h;
-    h.x = decode_e4m3x2(static_cast<uint16_t>(raw[i].x & 0xFFFF));
-    h.y = decode_e4m3x2(static_cast<uint16_t>(raw[i].x >> 16));
-    h.z = decode_e4m3x2(static_cast<uint16_t>(raw[i].y & 0xFFFF));
-    h.w = decode_e4m3x2(static_cast<uint16_t>(raw[i].y >> 16));
-    *reinterpret_cast<uint4 *>(&tile[hw + 32 * i][l16 * 4]) = h;
-  }
-  __syncthreads();
-
-  const int cp = tid & 63, tq = tid >> 6;
-  float m_lo = 0.0f, m_hi = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int t = tq * 16 + j;
-    const uint32_t w = tile[t][cp];
-    m_lo = fmaxf(m_lo, fabsf(__fmul_rn(f16_lo(w), srow[t])));
-    m_hi = fmaxf(m_hi, fabsf(__fmul_rn(f16_hi(w), srow[t])));
-  }
-  red[tq][2 * cp] = m_lo;
-  red[tq][2 * cp + 1] = m_hi;
-  __syncthreads();
-  if (tid < 128) {
-    float amax = red[0][tid];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i][tid]);
-    float s, inv;
-    group_scale(amax, kPow2, s, inv);
-    col_inv[tid] = inv;
-    sT[blockIdx.y * ld_sT + c0 + tid] = s;
-  }
-  __syncthreads();
-
-  const int cc = tid & 127, tq4 = tid >> 7;
-  const float inv = col_inv[cc];
-  uint32_t out[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float f[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int t = tq4 * 32 + 4 * j + e;
-      const uint32_t w = tile[t][cc >> 1];
-      const float x = __fmul_rn((cc & 1) ? f16_hi(w) : f16_lo(w), srow[t]);
-      f[e] = __fmul_rn(x, inv);
+  const int64_t ncb = C / 128;
+  const int64_t ntiles = ncb * (T / 128);
+  int pending[2] = {-1, -1};
+  auto issue_load = [&](int b, int64_t t) {
+    const uint32_t bar = smem_u32(&full[b]);
+    mbar_arrive_expect_tx(bar, kTileBytesQ8);
+    tma_load_2d(raw0 + b * kTileBytesQ8, &tmQ, bar, static_cast<int32_t>((t % ncb) * 128),
+                static_cast<int32_t>((t / ncb) * 128));
+  };
+  auto row_scale = [&](int64_t t) {  // threads < 128: this tile's scale of token row tid
+    return s_rows[(t % ncb) * ld_s_rows + (t / ncb) * 128 + tid];
+  };
+  if (tid == 0) {
+    mbar_init(smem_u32(&full[0]), 1);
+    mbar_init(smem_u32(&full[1]), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    for (int b = 0; b < 2; ++b) {
+      const int64_t t = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
+      if (t < ntiles) {
+        issue_load(b, t);
+        pending[b] = 0;
+      }
     }
-    out[j] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
   }
-  uint4 *dst = reinterpret_cast<uint4 *>(qT + (c0 + cc) * ldqT + t0 + tq4 * 32);
-  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  float sr_next = 0.0f;
+  if (tid < 128 && static_cast<int64_t>(blockIdx.x) < ntiles) sr_next = row_scale(blockIdx.x);
+  __syncthreads();
+
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t h = static_cast<uint32_t>(warp >> 3), j = static_cast<uint32_t>(warp & 7);
+  const int cw = 8 * warp + (lane >> 2);  // this thread's channel within the tile
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    const int buf = it & 1;
+    const bool got = mbar_wait_bounded(smem_u32(&full[buf]), (it >> 1) & 1, &abort_flag,
+                                       &g_quant_status, timeout_ns, FP8Q_ERR_TIMEOUT);
+    if (__syncthreads_or(!got)) {
+      if (tid == 0) {
+        for (int b = 0; b < 2; ++b)
+          if (pending[b] >= 0) mbar_wait_drain(smem_u32(&full[b]), pending[b]);
+        bulk_wait_group_all();
+      }
+      return;
+    }
+    if (tid == 0) pending[buf] = -1;
+    const int64_t c0 = (t % ncb) * 128, t0 = (t / ncb) * 128;
+    if (tid < 128) {
+      srow[tid] = sr_next;
+      if (t + gridDim.x < ntiles) sr_next = row_scale(t + gridDim.x);
+    }
+    // decode: thread (hw, l16) takes 8 codes of token rows hw + 32 i
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t r = static_cast<uint32_t>(hw + 32 * i);
+      uint2 q8;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                   : "=r"(q8.x), "=r"(q8.y)
+                   : "r"(raw0 + buf * kTileBytesQ8 + r * 128u + 8u * l16));
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                       tin + (l16 >> 3) * kHalfBytesBF16 + swz128(r, static_cast<uint32_t>(l16 & 7))),
+                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.x & 0xFFFF))),
+                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.x >> 16))),
+                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.y & 0xFFFF))),
+                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.y >> 16)))
+                   : "memory");
+    }
+    __syncthreads();  // FP16 tile and row scales ready; raw buffer `buf` consumed
+    if (tid == 0) {
+      const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
+      if (tn < ntiles) {
+        fence_proxy_async_shared();  // generic-proxy reads above, async-proxy write below
+        issue_load(buf, tn);
+        pending[buf] = ((it + 2) >> 1) & 1;
+      }
+    }
+
+    // this thread: channel cw, tokens 8m + 2(lane%4), +1 (m = 0..15)
+    float x[32];
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      uint32_t r4[4];
+      ldmatrix_x4_trans(tin + h * kHalfBytesBF16 + swz128(32u * qd + lane, j), r4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 4 * qd + e;
+        const float2 sr = *reinterpret_cast<const float2 *>(&srow[8 * m + 2 * (lane & 3)]);
+        x[2 * m] = __fmul_rn(f16_lo(r4[e]), sr.x);
+        x[2 * m + 1] = __fmul_rn(f16_hi(r4[e]), sr.y);
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    float sc, inv;
+    group_scale(amax, kPow2, sc, inv);
+    if ((lane & 3) == 0) sT[(t0 / 128) * ld_sT + c0 + cw] = sc;
+
+    if (tid == 0) bulk_wait_group_read<1>();  // stage `buf`: its store two tiles ago has read it
+    __syncthreads();  // every thread is done with the FP16 tile and row scales
+    const uint32_t stg = st0 + buf * kTileBytesQ8;
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+      st_shared_u16(stg + swz128(static_cast<uint32_t>(cw), static_cast<uint32_t>(m >> 1)) +
+                        8u * (m & 1) + 2u * (lane & 3),
+                    pack_e4m3x2(__fmul_rn(x[2 * m], inv), __fmul_rn(x[2 * m + 1], inv)));
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_2d(&tmQT, stg, static_cast<int32_t>(t0), static_cast<int32_t>(c0));
+      bulk_commit_group();
+    }
+  }
+  if (tid == 0) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ 128x128
@@ -592,6 +654,32 @@ fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX,
   return launch_status();
 }
 
+constexpr size_t kRequantSmem = 2 * kTileBytesQ8 + kTileBytesBF16 + 2 * kTileBytesQ8 + 1024;
+constexpr int kRequantCtasPerSm = 2;
+
+template <bool kPow2>
+fp8q_status launch_requant(unsigned grid, cudaStream_t s, const CUtensorMap &tmQ,
+                           const CUtensorMap &tmQT, int64_t T, int64_t C, const float *s_rows,
+                           int64_t ld_s_rows, float *sT, int64_t ld_sT, uint64_t timeout_ns) {
+  auto kern = requant_act_T_kernel<kPow2>;
+  static bool attr_set[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kRequantSmem)) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+  }
+  kern<<<grid, kTileThreads, kRequantSmem, s>>>(tmQ, tmQT, T, C, s_rows, ld_s_rows, sT, ld_sT,
+                                                timeout_ns);
+  return launch_status();
+}
+
 constexpr size_t kWeightTSmem = kTileBytesBF16 + kTileBytesQ + 1024;  // transposed path only
 
 template <bool kPow2, bool kTrans>
@@ -761,17 +849,22 @@ extern "C" fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, i
     return FP8Q_ERR_ALIGN;
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  const dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(T / 128));
+  CUtensorMap tmQ, tmQT;  // codes [T][C] and qT [C][T], 128 x 128-byte boxes
+  if (!make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, static_cast<uint64_t>(T),
+                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldq), 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_tmap_2d(&tmQT, CU_TENSOR_MAP_DATA_TYPE_UINT8, qT, static_cast<uint64_t>(C),
+                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return FP8Q_ERR_CUDA;
+  const int64_t ntiles = (C / 128) * (T / 128);
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * kRequantCtasPerSm;
+  const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
   auto s = static_cast<cudaStream_t>(stream);
-  auto qp = static_cast<const uint8_t *>(q);
-  auto tp = static_cast<uint8_t *>(qT);
-  if (scale_mode == FP8Q_SCALE_POW2)
-    requant_act_T_kernel<true><<<grid, kTileThreads, 0, s>>>(qp, ldq, s_rows, ld_s_rows, tp, ldqT,
-                                                             sT, ld_sT);
-  else
-    requant_act_T_kernel<false><<<grid, kTileThreads, 0, s>>>(qp, ldq, s_rows, ld_s_rows, tp,
-                                                              ldqT, sT, ld_sT);
-  return launch_status();
+  const uint64_t tmo = wait_timeout_ns().load();
+  return scale_mode == FP8Q_SCALE_POW2
+             ? launch_requant<true>(grid, s, tmQ, tmQT, T, C, s_rows, ld_s_rows, sT, ld_sT, tmo)
+             : launch_requant<false>(grid, s, tmQ, tmQT, T, C, s_rows, ld_s_rows, sT, ld_sT, tmo);
 }
 
 static int64_t tensor_partials(int64_t M) { return M > 0 ? (M + kTensorRows - 1) / kTensorRows : 1; }
