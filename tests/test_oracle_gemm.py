@@ -130,3 +130,38 @@ def test_tolerance_helper(oracle):
     assert np.array_equal(t, [2.0 ** -8, 2.0 ** -8, 2.0 ** -7])
     t = oracle.gemm_tolerance(np.array([1.0]), np.array([10.0]), False)
     assert t[0] == pytest.approx(2e-3)
+
+
+def _per_tensor_gemm(oracle, x, w, pow2):
+    M, K = x.shape
+    N = w.shape[0]
+    qx, sx = oracle.quant_tensor(x, pow2)
+    qw, sw = oracle.quant_tensor(w, pow2)
+    c, _ = oracle.gemm_rows(qx, np.full((K // 128, M), sx, np.float32), qw,
+                            np.full(((N + 127) // 128, K // 128), sw, np.float32),
+                            oracle.BSCALE_BLOCK)
+    return c
+
+
+def test_gemm_error_fine_grained_vs_per_tensor(oracle):
+    # GEMM-level comparison on the tiny Fprop inputs (0.1 % x100 outliers),
+    # both against an unquantised BF16 product in double.  With FP32 scales the
+    # 1x128 / 128x128 grouping lowers the error; with power-of-two scales a
+    # finer scale only shifts exponents, so while every value stays in E4M3's
+    # normal range the two give the same codes' relative precision.
+    x = synth.activation(256, 512, seed=0, name="tiny.X")
+    w = synth.weight(256, 512, seed=0, name="tiny.W")
+    ref = oracle.bf16_gemm_rows(x, w)
+
+    def rel(c):
+        return np.linalg.norm(c - ref) / np.linalg.norm(ref)
+
+    err = {}
+    for pow2 in (False, True):
+        qa, sa = oracle.quant_act(x, pow2)
+        qb, sb = oracle.quant_weight(w, pow2)
+        fine, _ = oracle.gemm_rows(qa, sa, qb, sb, oracle.BSCALE_BLOCK)
+        err[pow2] = (rel(fine), rel(_per_tensor_gemm(oracle, x, w, pow2)))
+    assert err[False][0] < 0.8 * err[False][1]
+    assert err[True][0] <= err[True][1] * (1 + 1e-9)
+    assert all(e < 0.1 for pair in err.values() for e in pair)
