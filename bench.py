@@ -383,13 +383,16 @@ class LinearBwd(Workload):
 
 
 class MoEFprop(Workload):
-    def __init__(self, G=16, tokens=16384, d_model=7168, d_ff=4096, d_down_in=2048):
-        self.name = f"moe_fprop_{G}x{tokens}"
+    def __init__(self, G=16, tokens=16384, d_model=7168, d_ff=4096, d_down_in=2048, pow2=False):
+        self.name = f"moe_fprop_pow2_{G}x{tokens}" if pow2 else f"moe_fprop_{G}x{tokens}"
+        self.pow2 = pow2
         self.G, self.T, self.dm, self.dff, self.ddi = G, tokens, d_model, d_ff, d_down_in
         self.config = {"experts": G, "tokens": tokens, "up": f"{d_model}->{d_ff}",
                        "down": f"{d_down_in}->{d_model}", "routing": "Dirichlet(0.5) top-1",
                        "step": "quant_act(X) + quant_weight(W_up, all experts) + grouped GEMM "
-                               "up; quant_act(H) + quant_weight(W_down) + grouped GEMM down"}
+                               "up; quant_act(H) + quant_weight(W_down) + grouped GEMM down" +
+                               ("; power-of-two scales, GEMMs on the block-scaled MMA"
+                                if pow2 else "")}
 
     def host_inputs(self):
         from fp8_fine_grained_amax_gb300 import synth
@@ -421,21 +424,27 @@ class MoEFprop(Workload):
     def kernels(self, st, stream):
         from fp8_fine_grained_amax_gb300 import binding as B
         G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
+        mode = B.FP8Q_SCALE_POW2 if self.pow2 else B.FP8Q_SCALE_FP32
+        ggemm = B.fp8q_grouped_gemm_pow2 if self.pow2 else B.fp8q_grouped_gemm
+        gname = "fp8q_gemm_mx_kernel" if self.pow2 else "fp8q_gemm_kernel"
         return [
             Kernel("quant_act_kernel(X)", lambda: B.fp8q_quant_act(
-                st["X"], q=st["qx"], sa=st["sx"], stream=stream), T * dm * 3 + T * dm // 32, "hbm"),
+                st["X"], q=st["qx"], sa=st["sx"], scale_mode=mode, stream=stream),
+                T * dm * 3 + T * dm // 32, "hbm"),
             Kernel("quant_weight_kernel(Wup)", lambda: B.fp8q_quant_weight(
-                st["Wup"], q=st["qup"], sb=st["sup"], stream=stream), G * dff * dm * 3, "hbm"),
-            Kernel("fp8q_gemm_kernel(grouped up)", lambda: B.fp8q_grouped_gemm(
+                st["Wup"], q=st["qup"], sb=st["sup"], scale_mode=mode, stream=stream),
+                G * dff * dm * 3, "hbm"),
+            Kernel(gname + "(grouped up)", lambda: ggemm(
                 st["qx"], st["sx"], st["qup"].view(G, dff, dm),
                 st["sup"].view(G, dff // 128, dm // 128), st["offs"], c=st["Yup"],
                 stream=stream), 2.0 * T * dff * dm, "tensor"),
             Kernel("quant_act_kernel(H)", lambda: B.fp8q_quant_act(
-                st["H"], q=st["qh"], sa=st["sh"], stream=stream), T * ddi * 3 + T * ddi // 32,
-                "hbm"),
+                st["H"], q=st["qh"], sa=st["sh"], scale_mode=mode, stream=stream),
+                T * ddi * 3 + T * ddi // 32, "hbm"),
             Kernel("quant_weight_kernel(Wdown)", lambda: B.fp8q_quant_weight(
-                st["Wdown"], q=st["qdn"], sb=st["sdn"], stream=stream), G * dm * ddi * 3, "hbm"),
-            Kernel("fp8q_gemm_kernel(grouped down)", lambda: B.fp8q_grouped_gemm(
+                st["Wdown"], q=st["qdn"], sb=st["sdn"], scale_mode=mode, stream=stream),
+                G * dm * ddi * 3, "hbm"),
+            Kernel(gname + "(grouped down)", lambda: ggemm(
                 st["qh"], st["sh"], st["qdn"].view(G, dm, ddi),
                 st["sdn"].view(G, dm // 128, ddi // 128), st["offs"], c=st["Ydn"],
                 stream=stream), 2.0 * T * dm * ddi, "tensor"),
@@ -445,10 +454,11 @@ class MoEFprop(Workload):
         import oracle
         G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
         t0 = time.perf_counter()
-        qx, sx = oracle.quant_act(inp["X"])
-        qh, sh = oracle.quant_act(inp["H"])
-        qup, sup = oracle.quant_weight(inp["Wup"])
-        qdn, sdn = oracle.quant_weight(inp["Wdown"])
+        p2 = self.pow2
+        qx, sx = oracle.quant_act(inp["X"], p2)
+        qh, sh = oracle.quant_act(inp["H"], p2)
+        qup, sup = oracle.quant_weight(inp["Wup"], p2)
+        qdn, sdn = oracle.quant_weight(inp["Wdown"], p2)
         t_q = time.perf_counter() - t0
         budget = (target_s - t_q) / 2
         offs = inp["offs"]
@@ -611,6 +621,8 @@ def make_workload(name: str) -> Workload:
         return LinearBwd()
     if name == "moe_fprop_16x16384":
         return MoEFprop()
+    if name == "moe_fprop_pow2_16x16384":
+        return MoEFprop(pow2=True)
     if name == "linear_bwd_cached_T8192":
         return LinearBwdCached()
     for kind in ("quant_act_pow2", "quant_act_T", "quant_tensor", "quant_act"):

@@ -54,6 +54,8 @@ SIGNATURES = {
                                     _I64, _I64, _P]),
     "fp8q_grouped_gemm": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _INT, _P, _I64, _INT,
                                  _I64, _I64, _I64, _P]),
+    "fp8q_grouped_gemm_pow2": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _INT, _P, _I64, _INT,
+                                      _I64, _I64, _I64, _P]),
     "fp8q_cast_e4m3": (_INT, [_P, _I64, _P, _P]),
     "fp8q_sync_status": (_INT, [_P]),
     "fp8q_set_wait_timeout_ns": (None, [_U64]),
@@ -277,7 +279,8 @@ def fp8q_gemm_pow2_accumulate(a, sa, b, sb, c, *, bscale_kind=FP8Q_BSCALE_BLOCK,
                                 _entry="fp8q_gemm_pow2_accumulate")
 
 
-def fp8q_grouped_gemm(a, sa, b, sb, offs, *, out_dtype=FP8Q_OUT_BF16, c=None, stream=None):
+def fp8q_grouped_gemm(a, sa, b, sb, offs, *, out_dtype=FP8Q_OUT_BF16, c=None, stream=None,
+                      _entry="fp8q_grouped_gemm"):
     """MoE grouped GEMM: a [M][K], b [G][N][K], sb [G][ceil(N/128)][K/128],
     offs int32 [G+1] on the device.  Rows outside [offs[0], offs[G]) are left as is."""
     M, K = a.shape
@@ -287,11 +290,17 @@ def fp8q_grouped_gemm(a, sa, b, sb, offs, *, out_dtype=FP8Q_OUT_BF16, c=None, st
         c = torch.empty((M, N), dtype=dt, device=a.device)
     if b.stride(2) != 1 or b.stride(0) != N * b.stride(1):
         raise ValueError("b must be [G][N][ldb] with experts packed back to back")
-    _check(load_library().fp8q_grouped_gemm(
+    _check(getattr(load_library(), _entry)(
         _ptr(a), _rows_ld(a, "a") if a.numel() else K, _ptr(sa),
         _rows_ld(sa, "sa") if sa.numel() else M, _ptr(b), b.stride(1), _ptr(sb), _ptr(offs), G,
-        _ptr(c), _rows_ld(c, "c"), out_dtype, M, N, K, _stream(stream)), "fp8q_grouped_gemm")
+        _ptr(c), _rows_ld(c, "c"), out_dtype, M, N, K, _stream(stream)), _entry)
     return c
+
+
+def fp8q_grouped_gemm_pow2(a, sa, b, sb, offs, *, out_dtype=FP8Q_OUT_BF16, c=None, stream=None):
+    """fp8q_grouped_gemm for power-of-two scales on the block-scaled MMA."""
+    return fp8q_grouped_gemm(a, sa, b, sb, offs, out_dtype=out_dtype, c=c, stream=stream,
+                             _entry="fp8q_grouped_gemm_pow2")
 
 
 def fp8q_cast_e4m3(x, *, q=None, stream=None):

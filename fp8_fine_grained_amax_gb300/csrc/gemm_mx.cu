@@ -98,6 +98,8 @@ struct MxArgs {
   int M, N;
   int num_kb;
   int tiles_m, tiles_n;
+  const int32_t *offs;  // grouped only: expert row offsets [G + 1] (device)
+  int G;
   uint64_t timeout_ns;
 };
 
@@ -113,6 +115,8 @@ struct alignas(8) MxCtl {
   int abort_flag;
 };
 
+constexpr int kMaxGroups = 1024;
+constexpr size_t kGroupTables = 3 * (kMaxGroups + 1) * sizeof(int);
 constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(MxCtl);
 
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -138,22 +142,49 @@ __device__ __forceinline__ uint32_t ue8m0_of(float s, bool &bad) {
 }
 
 struct MxTile {
-  int m0;  // first row of the pair tile
-  int n0;  // first column
+  int m0;       // first row of the pair tile (of A and of C)
+  int row_end;  // rows >= row_end are not stored (the expert's end, or M)
+  int b_row;    // first row of B (expert g's rows start at g * N)
+  int n0;       // first column
+  int g;        // expert (grouped) or 0
 };
 
-__device__ __forceinline__ MxTile mx_tile_of(int t, const MxArgs &p) {
-  const int band_tiles = kGroupM * p.tiles_n;
-  const int band = t / band_tiles, within = t - band * band_tiles;
-  const int mt0 = band * kGroupM;
-  const int rows = min(kGroupM, p.tiles_m - mt0);
+// Dense: bands of kGroupM m-tiles for L2 reuse.  Grouped: expert-major, m-tiles
+// fastest; s_lo / s_hi = clamped row range of expert g, s_pre[g] = m-tiles of
+// the experts before g.
+template <bool kGrouped>
+__device__ __forceinline__ MxTile mx_tile_of(int t, const MxArgs &p, const int *s_lo,
+                                             const int *s_hi, const int *s_pre) {
   MxTile r;
-  r.m0 = (mt0 + within % rows) * kTileM;
-  r.n0 = (within / rows) * BN;
+  if (!kGrouped) {
+    const int band_tiles = kGroupM * p.tiles_n;
+    const int band = t / band_tiles, within = t - band * band_tiles;
+    const int mt0 = band * kGroupM;
+    const int rows = min(kGroupM, p.tiles_m - mt0);
+    r.m0 = (mt0 + within % rows) * kTileM;
+    r.row_end = p.M;
+    r.n0 = (within / rows) * BN;
+    r.b_row = r.n0;
+    r.g = 0;
+  } else {
+    int lo = 0, hi = p.G;  // largest g with s_pre[g] * tiles_n <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] * p.tiles_n <= t) lo = mid; else hi = mid;
+    }
+    const int g = lo;
+    const int mtiles = s_pre[g + 1] - s_pre[g];
+    const int local = t - s_pre[g] * p.tiles_n;
+    r.m0 = s_lo[g] + (local % mtiles) * kTileM;
+    r.row_end = s_hi[g];
+    r.n0 = (local / mtiles) * BN;
+    r.b_row = g * p.N + r.n0;
+    r.g = g;
+  }
   return r;
 }
 
-template <int kBScale, bool kOutF32, bool kAccum>
+template <int kBScale, bool kOutF32, bool kAccum, bool kGrouped = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8q_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const MxArgs p) {
@@ -163,13 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sA = smem;
   uint8_t *sB = smem + kStages * kABytes;
   MxCtl *ctl = reinterpret_cast<MxCtl *>(smem + kRingBytes);
+  int *s_lo = reinterpret_cast<int *>(ctl + 1);  // grouped only (see mx_tile_of)
+  int *s_hi = s_lo + (kMaxGroups + 1);
+  int *s_pre = s_hi + (kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int *abort_flag = &ctl->abort_flag;
   const uint32_t rank = cluster_ctarank();  // 0 = the CTA that issues the MMAs
   const int tile_first = static_cast<int>(blockIdx.x >> 1);
   const int tile_step = static_cast<int>(gridDim.x >> 1);
-  const int total_tiles = p.tiles_m * p.tiles_n;
   const int nst = (p.num_kb + kGroupsPerStage - 1) / kGroupsPerStage;  // scale stages per tile
 
   if (threadIdx.x == 0) {
@@ -199,6 +232,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   cluster_sync_all();
+  // grouped: clamp the expert offsets into [0, M] and build the m-tile prefix
+  int total_tiles;
+  if (kGrouped) {
+    for (int g = threadIdx.x; g <= p.G; g += blockDim.x) s_lo[g] = min(max(p.offs[g], 0), p.M);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // ranges never overlap: an expert starts no earlier than the previous
+      // one ended, and a decreasing offset makes it empty
+      int acc = 0, prev_hi = 0;
+      for (int g = 0; g < p.G; ++g) {
+        const int lo = max(s_lo[g], prev_hi);
+        const int hi = max(lo, s_lo[g + 1]);
+        s_lo[g] = lo;
+        s_hi[g] = hi;
+        s_pre[g] = acc;
+        acc += (hi - lo + kTileM - 1) / kTileM;
+        prev_hi = hi;
+      }
+      s_pre[p.G] = acc;
+    }
+    __syncthreads();
+    total_tiles = s_pre[p.G] * p.tiles_n;
+  } else {
+    total_tiles = p.tiles_m * p.tiles_n;
+  }
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -231,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     : (BN / 128) * kGroupsPerStage;
     const int NB = (p.N + 127) / 128;
     auto load_raw = [&](int t, int js, float (&r)[kRaw]) {
-      const MxTile tl = mx_tile_of(t, p);
+      const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
       const int kb0 = js * kGroupsPerStage;
 #pragma unroll
       for (int i = 0; i < kRaw; ++i) r[i] = 1.0f;
@@ -253,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // columns past N in a partial block read zero-filled B rows, so the
         // block's own scale is as good as any for them
+        const float *sbg = kGrouped ? p.sb + static_cast<int64_t>(tl.g) * NB * p.num_kb : p.sb;
 #pragma unroll
         for (int h = 0; h < BN / 128; ++h) {
           const int nb = tl.n0 / 128 + h;
@@ -260,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kGroupsPerStage; ++j)
             if (kb0 + j < p.num_kb && nb < NB)
               r[4 * h + j] = kBScale == FP8Q_BSCALE_BLOCK
-                                 ? __ldg(p.sb + static_cast<int64_t>(nb) * p.ld_sb + kb0 + j)
+                                 ? __ldg(sbg + static_cast<int64_t>(nb) * p.ld_sb + kb0 + j)
                                  : __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + nb);
         }
       }
@@ -341,10 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf) * 8u);
 
-      const MxTile tl = mx_tile_of(t, p);
+      const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
       const int m = tl.m0 + row_in_tile;
       const int ncol0 = tl.n0 + col_half * kEpiCols;
-      if (m < p.M && ncol0 < p.N) {
+      if (m < tl.row_end && ncol0 < p.N) {
         const bool full = ncol0 + kEpiCols <= p.N;
         if (kOutF32) {
           float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
@@ -425,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0, armed_phase = 0;
       bool ok = true;
       for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
-        const MxTile tl = mx_tile_of(t, p);
+        const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1, abort_flag,
                                  &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
@@ -438,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmA, fb0, kb * BK,
                            tl.m0 + static_cast<int>(rank) * BM);
           tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &tmB, fb0, kb * BK,
-                           tl.n0 + static_cast<int>(rank) * (BN / 2));
+                           tl.b_row + static_cast<int>(rank) * (BN / 2));
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -532,10 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
-template <int kBScale, bool kOutF32, bool kAccum>
+template <int kBScale, bool kOutF32, bool kAccum, bool kGrouped = false>
 fp8q_status launch_mx(const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs &args,
                       int64_t tiles, cudaStream_t s) {
-  auto kern = fp8q_gemm_mx_kernel<kBScale, kOutF32, kAccum>;
+  auto kern = fp8q_gemm_mx_kernel<kBScale, kOutF32, kAccum, kGrouped>;
+  constexpr size_t smem = kSmemBytes + (kGrouped ? kGroupTables : 0);
   static int max_pairs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
@@ -547,7 +607,7 @@ fp8q_status launch_mx(const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -555,7 +615,7 @@ fp8q_status launch_mx(const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs
     std::lock_guard<std::mutex> lock(mu);
     if (max_pairs[dev] == 0) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmemBytes)) != cudaSuccess)
+                               static_cast<int>(smem)) != cudaSuccess)
         return FP8Q_ERR_CUDA;
       int n = 0;
       cfg.gridDim = dim3(2, 1, 1);
@@ -683,4 +743,58 @@ extern "C" fp8q_status fp8q_gemm_pow2_accumulate(const void *a, int64_t lda, con
                                                  int64_t K, void *stream) {
   return mx_entry(a, lda, sa, ld_sa, b, ldb, sb, ld_sb, bscale_kind, c, ldc, FP8Q_OUT_FP32, M, N,
                   K, stream, true);
+}
+
+extern "C" fp8q_status fp8q_grouped_gemm_pow2(const void *a, int64_t lda, const float *sa,
+                                              int64_t ld_sa, const void *b, int64_t ldb,
+                                              const float *sb, const int32_t *offs, int G,
+                                              void *c, int64_t ldc, int out_dtype, int64_t M,
+                                              int64_t N, int64_t K, void *stream) {
+  if (G < 1 || G > kMaxGroups) return FP8Q_ERR_SHAPE;
+  if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP32) return FP8Q_ERR_INVALID;
+  if (M < 0 || N < 0 || K < 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (M >= (1ll << 31) - kTileM || K >= (1ll << 31)) return FP8Q_ERR_SHAPE;
+  if (static_cast<int64_t>(G) * N >= (1ll << 31) - BN) return FP8Q_ERR_SHAPE;
+  if (ldc < N || ld_sa < M) return FP8Q_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8Q_OK;
+  if (!c || !offs) return FP8Q_ERR_INVALID;
+  const int64_t esz = out_dtype == FP8Q_OUT_FP32 ? 4 : 2;
+  if (!aligned16(c) || (ldc * esz) % 16 || !aligned4(offs)) return FP8Q_ERR_ALIGN;
+  auto st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  if (fp8q_status e = device_info(dev)) return e;
+  if (K == 0) return FP8Q_ERR_SHAPE;  // an expert's empty sum is not written by this path
+  if (lda < K || ldb < K) return FP8Q_ERR_SHAPE;
+  if (!a || !b || !sa || !sb) return FP8Q_ERR_INVALID;
+  if (!aligned16(a) || !aligned16(b) || lda % 16 || ldb % 16 || !aligned4(sa) || !aligned4(sb))
+    return FP8Q_ERR_ALIGN;
+  if (dev.max_smem_optin < static_cast<int>(kSmemBytes + kGroupTables)) return FP8Q_ERR_UNSUPPORTED;
+  const int64_t KB = K / 128;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K, lda, 128, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, static_cast<uint64_t>(G) * N, K, ldb,
+                    128, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+    return FP8Q_ERR_CUDA;
+  MxArgs args{};
+  args.sa = sa;
+  args.ld_sa = ld_sa;
+  args.sb = sb;
+  args.ld_sb = KB;
+  args.c = c;
+  args.ldc = ldc;
+  args.M = static_cast<int>(M);
+  args.N = static_cast<int>(N);
+  args.num_kb = static_cast<int>(KB);
+  args.tiles_m = static_cast<int>((M + kTileM - 1) / kTileM);
+  args.tiles_n = static_cast<int>((N + BN - 1) / BN);
+  args.offs = offs;
+  args.G = G;
+  args.timeout_ns = wait_timeout_ns().load();
+  // upper bound on tiles: each expert adds at most one partial m-tile
+  const int64_t bound = (static_cast<int64_t>(args.tiles_m) + G) * args.tiles_n;
+  if (bound >= (1ll << 31)) return FP8Q_ERR_SHAPE;
+  return out_dtype == FP8Q_OUT_FP32
+             ? launch_mx<FP8Q_BSCALE_BLOCK, true, false, true>(ta, tb, args, bound, st)
+             : launch_mx<FP8Q_BSCALE_BLOCK, false, false, true>(ta, tb, args, bound, st);
 }

@@ -268,6 +268,18 @@ fp8q_status fp8q_grouped_gemm(const void *a, int64_t lda, const float *sa,
                               int64_t N, int64_t K, void *stream);
 
 /*
+ * fp8q_grouped_gemm for power-of-two scales, on the block-scaled MMA (see
+ * fp8q_gemm_pow2): the same arguments, layouts and results, with the same
+ * precondition on the scales.  Tiles are 256 rows x 256 columns (a CTA pair);
+ * K must be a positive multiple of 128 (K == 0 returns FP8Q_ERR_SHAPE).
+ */
+fp8q_status fp8q_grouped_gemm_pow2(const void *a, int64_t lda, const float *sa,
+                                   int64_t ld_sa, const void *b, int64_t ldb,
+                                   const float *sb, const int32_t *offs, int G,
+                                   void *c, int64_t ldc, int out_dtype, int64_t M,
+                                   int64_t N, int64_t K, void *stream);
+
+/*
  * Plain FP32 -> E4M3 conversion of n values (round to nearest-even, saturate
  * to +-448, NaN -> 0x7F), with no scaling.  The quantisers use the same
  * conversion; this entry exposes it so it can be checked on every FP32 bit

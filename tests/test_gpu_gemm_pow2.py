@@ -189,3 +189,59 @@ def test_pow2_rejects_other_scales_through_the_status_word():
     B.fp8q_gemm_pow2(qa, sa, qb, sb)
     assert B.fp8q_sync_status() == B.FP8Q_ERR_INVALID
     assert B.fp8q_sync_status() == 0
+
+
+def _moe_pow2(oracle, offs, N, K, seed):
+    G = offs.size - 1
+    M = int(offs[-1])
+    x = synth.activation(M, K, seed=seed, name="p2moe.X")
+    ws = [synth.weight(N, K, seed=seed + 1 + g, name=f"p2moe.W{g}") for g in range(G)]
+    qa, sa = B.fp8q_quant_act(bf16_to_torch(x), scale_mode=P2)
+    qb = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+    sb = torch.empty((G, (N + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+    for g in range(G):
+        B.fp8q_quant_weight(bf16_to_torch(ws[g]), q=qb[g], sb=sb[g], scale_mode=P2)
+    torch.cuda.synchronize()
+    qa_r, sa_r = oracle.quant_act(x, True)
+    qb_r = np.stack([oracle.quant_weight(wg, True)[0] for wg in ws])
+    sb_r = np.stack([oracle.quant_weight(wg, True)[1] for wg in ws])
+    assert_bytes_equal(u8(qb), qb_r, "expert codes")
+    assert_scales_equal(f32(sa), sa_r, "A scales")
+    return (qa, sa, qb, sb), (qa_r, sa_r, qb_r, sb_r)
+
+
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_pow2_grouped_small(oracle, out):
+    offs = np.array([0, 77, 77, 300, 301, 555], np.int32)   # one empty, one single-row expert
+    N, K = 264, 384
+    (qa, sa, qb, sb), (qa_r, sa_r, qb_r, sb_r) = _moe_pow2(oracle, offs, N, K, 21)
+    M = int(offs[-1])
+    od = B.FP8Q_OUT_BF16 if out == "bf16" else B.FP8Q_OUT_FP32
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    c = torch.full((M + 5, N), 3.0, dtype=dt, device="cuda")   # rows past offs[G] untouched
+    a_pad = torch.cat([qa, torch.zeros((5, K), dtype=torch.uint8, device="cuda")])
+    sa_pad = torch.cat([sa, torch.ones((K // 128, 5), device="cuda")], dim=1).contiguous()
+    B.fp8q_grouped_gemm_pow2(a_pad, sa_pad, qb, sb, torch.from_numpy(offs).cuda(), out_dtype=od,
+                             c=c)
+    torch.cuda.synchronize()
+    ref, ad = oracle.grouped_gemm_rows(qa_r, sa_r, qb_r, sb_r, offs)
+    _check(c[:M], ref, ad, out == "bf16", "pow2 grouped small")
+    assert torch.all(c[M:] == 3.0)
+
+
+def test_pow2_grouped_moe_workload_sampled(oracle):
+    # MoE up-projection with power-of-two scales: 16 experts, 16384 tokens,
+    # Dirichlet(0.5) top-1 routing, K=7168 -> N=4096; sampled rows of every expert
+    offs = synth.moe_offsets(16384, 16, 0.5, seed=0)
+    N, K = 4096, 7168
+    (qa, sa, qb, sb), (qa_r, sa_r, qb_r, sb_r) = _moe_pow2(oracle, offs, N, K, 0)
+    c = B.fp8q_grouped_gemm_pow2(qa, sa, qb, sb, torch.from_numpy(offs).cuda())
+    torch.cuda.synchronize()
+    rows = set()
+    for g in range(16):
+        lo, hi = int(offs[g]), int(offs[g + 1])
+        if hi > lo:
+            rows |= {lo, hi - 1, (lo + hi) // 2}
+    rows = np.array(sorted(rows), np.int64)
+    ref, ad = oracle.grouped_gemm_rows(qa_r, sa_r, qb_r, sb_r, offs, rows)
+    _check(c[torch.from_numpy(rows).cuda()], ref, ad, True, "pow2 moe up-proj")
