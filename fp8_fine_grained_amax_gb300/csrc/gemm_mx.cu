@@ -14,27 +14,31 @@
 // product as the FP32-scale path's, accumulated over the whole K in the FP32
 // TMEM accumulator with no per-group fold by the CUDA cores.
 //
-// Roles (384 threads; CTA pairs, tile 256 x 224, one MMA thread per pair):
-//   warp 0      TMA producer: this CTA's 128 rows of A and 112 rows of B per
+// Roles (384 threads; CTA pairs, tile 256 x BN, one MMA thread per pair):
+//   warp 0      TMA producer: this CTA's 128 rows of A and BN/2 rows of B per
 //               K-group into a kStages ring, completing on the leading CTA's
 //               "full" barrier.
 //   warp 1      MMA issuer (leading CTA): per K-group 4 x tcgen05.mma
-//               .cta_group::2 .kind::mxf8f6f4 .block_scale (M=256, N=224,
-//               K=32) into one of two TMEM accumulators (columns 0-223 and
-//               224-447, alternating by tile), reading the scale exponents of
-//               the current scale stage.
-//   warps 4-11  scale producers and epilogue.  Scale stage s (TMEM columns
-//               448 + 16 s .. +15, 4 stages) holds the exponents of four
-//               consecutive K-groups, one byte per group: warps 4-7 write the
-//               A exponents of their rows (column +q for lane quarter q),
-//               warps 8-11 the B exponents of the tile's 224 columns (columns
-//               +8..+14, the same in every lane quarter).  They drain a
-//               tile's accumulator (each thread 112 columns of its row) while
-//               the tensor cores fill the other one, and store C.
+//               .cta_group::2 .kind::mxf8f6f4 .block_scale (M=256, N=BN,
+//               K=32) into one of kAccBufs TMEM accumulators (BN columns each,
+//               alternating by tile), reading the scale exponents of the
+//               current scale stage.
+//   warps 4-11  scale producers and epilogue.  The TMEM columns after the
+//               accumulators hold kSfStages scale stages of 16 columns, each
+//               with the exponents of four consecutive K-groups, one byte per
+//               group: warps 4-7 write the A exponents of their rows (column
+//               +q for lane quarter q), warps 8-11 the B exponents of the
+//               tile's BN columns (columns +8.., the same in every lane
+//               quarter).  At the end of a tile they read its accumulator
+//               (each thread BN/2 columns of its row), release it and store C.
 //
-// 224-column tiles divide the model widths 7168 exactly and leave TMEM room
-// for two accumulators plus the scale ring, so the tensor cores never wait
-// for an accumulator to be read out.
+// Shipped shape: BN = 256 with one accumulator (columns 0-255) and 16 scale
+// stages (columns 256-511).  The epilogue writes scale stages up to 6 ahead
+// into the next tile before it drains the current one; with two
+// accumulators (any BN that is a multiple of 128 and fits) it drains tile t-1
+// while the tensor cores fill tile t.  Narrower tiles measured slower: a
+// 224-wide MMA takes about as long as a 256-wide one, and 256 x 128 tiles with
+// two accumulators lose more to per-group overhead than they gain.
 // A scale that is not a power of two (2^-127 .. 2^127) is a caller error: the
 // kernel uses its exponent and records FP8Q_ERR_INVALID in its status word.
 // Every wait is bounded in time (as in the FP32-scale GEMM).
@@ -85,6 +89,10 @@ static_assert(BN % 128 == 0 && kEpiCols % 16 == 0,
 constexpr int kRunAhead = kAccBufs == 1 ? 6 : kSfStages;
 static_assert(kAccCols + kSfStages * kSfStageCols <= kTmemCols, "TMEM budget");
 constexpr int kGroupsPerStage = 4;              // one byte per K-group in a 32-bit cell
+// Scale producers: true = warps 4-7 write A exponents and warps 8-11 B
+// exponents; false = warps 4-7 write both (warps 8-11 only drain).
+constexpr bool kSplitSides = true;
+constexpr int kProducerWarps = kSplitSides ? 8 : 4;
 constexpr int kGroupM = 16;                     // L2 rasterisation band (m-tiles)
 constexpr uint64_t kDrainNs = 1000000000ull;
 
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->empty[i]), 1);
     }
     for (int i = 0; i < kSfStages; ++i) {
-      mbar_init(smem_u32(&ctl->sfull[i]), 2 * kEpiWarps);
+      mbar_init(smem_u32(&ctl->sfull[i]), 2 * kProducerWarps);
       mbar_init(smem_u32(&ctl->sempty[i]), 1);
     }
     for (int i = 0; i < kAccBufs; ++i) {
@@ -265,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================== scale producers + epilogue
     const int ew = warp - 4;
     const int q = warp & 3;          // lane quarter this warp may access
-    const bool a_side = ew < 4;      // warps 4-7: A exponents; 8-11: B exponents
+    const bool producer = kSplitSides || ew < 4;
+    const bool do_a = producer && (!kSplitSides || ew < 4);   // writes A exponents
+    const bool do_b = producer && (!kSplitSides || ew >= 4);  // writes B exponents
     const int col_half = ew >> 2;    // epilogue: columns [kEpiCols * col_half, +kEpiCols)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
@@ -285,20 +295,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   B warps, per-column scales: raw[4 c + j] = sb of column n0 + 32 c + lane.
     //   B warps, block scales: raw[4 h + j] = the scale of 128-column block h
     //   of the tile (column group c lies in block c / 4).
-    constexpr int kRaw = kBScale == FP8Q_BSCALE_ROW ? kBCols32 * kGroupsPerStage
-                                                    : (BN / 128) * kGroupsPerStage;
+    constexpr int kRawB = kBScale == FP8Q_BSCALE_ROW ? kBCols32 * kGroupsPerStage
+                                                     : (BN / 128) * kGroupsPerStage;
+    // split: a warp loads one side, from raw[0]; combined: A at [0, 4), B after
+    constexpr int kOffB = kSplitSides ? 0 : kGroupsPerStage;
+    constexpr int kRaw = kSplitSides ? (kRawB > kGroupsPerStage ? kRawB : kGroupsPerStage)
+                                     : kGroupsPerStage + kRawB;
     const int NB = (p.N + 127) / 128;
     auto load_raw = [&](int t, int js, float (&r)[kRaw]) {
       const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
       const int kb0 = js * kGroupsPerStage;
 #pragma unroll
       for (int i = 0; i < kRaw; ++i) r[i] = 1.0f;
-      if (a_side) {
+      if (do_a) {
         const int m = tl.m0 + row_in_tile;
 #pragma unroll
         for (int j = 0; j < kGroupsPerStage; ++j)
           if (kb0 + j < p.num_kb && m < p.M)
             r[j] = __ldg(p.sa + static_cast<int64_t>(kb0 + j) * p.ld_sa + m);
+        if (kSplitSides) return;
+      }
+      float *rb = r + kOffB;
+      if (!do_b) {
       } else if (kBScale == FP8Q_BSCALE_ROW) {
 #pragma unroll
         for (int c = 0; c < kBCols32; ++c) {
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kGroupsPerStage; ++j)
             if (kb0 + j < p.num_kb && n < p.N)
-              r[4 * c + j] = __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + n);
+              rb[4 * c + j] = __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + n);
         }
       } else {
         // columns past N in a partial block read zero-filled B rows, so the
@@ -318,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kGroupsPerStage; ++j)
             if (kb0 + j < p.num_kb && nb < NB)
-              r[4 * h + j] = kBScale == FP8Q_BSCALE_BLOCK
-                                 ? __ldg(sbg + static_cast<int64_t>(nb) * p.ld_sb + kb0 + j)
-                                 : __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + nb);
+              rb[4 * h + j] = kBScale == FP8Q_BSCALE_BLOCK
+                                  ? __ldg(sbg + static_cast<int64_t>(nb) * p.ld_sb + kb0 + j)
+                                  : __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + nb);
         }
       }
     };
@@ -335,6 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         nt += tile_step;
         njs = 0;
       }
+      if (!producer) {  // only walks the cursor, in step with the producers
+        cur_t = nt;
+        cur_js = njs;
+        return true;
+      }
       float nxt[kRaw];
       if (nt < total_tiles) load_raw(nt, njs, nxt);
       const bool got = mbar_wait_bounded(smem_u32(&ctl->sempty[ss]), sphase ^ 1, abort_flag,
@@ -343,23 +366,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t col = kAccCols + static_cast<uint32_t>(ss) * kSfStageCols;
       bool bad = false;
-      if (a_side) {
+      if (do_a) {
         uint32_t w = 0;
 #pragma unroll
         for (int j = 0; j < kGroupsPerStage; ++j) w |= ue8m0_of(raw[j], bad) << (8 * j);
         tmem_st_32x32b_x1(tmem_base + lane_addr + col + static_cast<uint32_t>(q), w);
-      } else {
+      }
+      if (do_b && !(kSplitSides && do_a)) {
         uint32_t w[8];
+        if (kBScale == FP8Q_BSCALE_ROW) {  // one word per 32-column group
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t word = 0x7F7F7F7Fu;  // column group past the tile: unused, 2^0
-          if (c < kBCols32) {
-            const int base = kBScale == FP8Q_BSCALE_ROW ? 4 * c : 4 * (c / 4);
-            word = 0;
+          for (int c = 0; c < 8; ++c) {
+            uint32_t word = 0x7F7F7F7Fu;  // column group past the tile: unused, 2^0
+            if (c < kBCols32) {
+              word = 0;
 #pragma unroll
-            for (int j = 0; j < kGroupsPerStage; ++j) word |= ue8m0_of(raw[base + j], bad) << (8 * j);
+              for (int j = 0; j < kGroupsPerStage; ++j)
+                word |= ue8m0_of(raw[kOffB + 4 * c + j], bad) << (8 * j);
+            }
+            w[c] = word;
           }
-          w[c] = word;
+        } else {  // one word per 128-column block, repeated for its 4 column groups
+          uint32_t wb[BN / 128];
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < kGroupsPerStage; ++j)
+              word |= ue8m0_of(raw[kOffB + 4 * h + j], bad) << (8 * j);
+            wb[h] = word;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) w[c] = c < kBCols32 ? wb[c / 4] : 0x7F7F7F7Fu;
         }
         tmem_st_32x32b_x8(tmem_base + lane_addr + col + kSfbOffset, w);
       }
@@ -388,30 +426,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tphase ^= 1u << buf;
       tc_fence_after();
       constexpr int kChunks = kEpiCols / 16;
-      uint32_t v[kChunks][16];
       const uint32_t taddr = tmem_base + lane_addr +
                              static_cast<uint32_t>(buf * BN + col_half * kEpiCols);
-#pragma unroll
-      for (int i = 0; i < kChunks; ++i) tmem_ld_32x32b_x16(taddr + i * 16, v[i]);
-      tmem_wait_ld_tied(v[0]);
-#pragma unroll
-      for (int i = 1; i < kChunks; ++i) reg_tie(v[i]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf) * 8u);
-
       const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
       const int m = tl.m0 + row_in_tile;
       const int ncol0 = tl.n0 + col_half * kEpiCols;
-      if (m < tl.row_end && ncol0 < p.N) {
-        const bool full = ncol0 + kEpiCols <= p.N;
-        if (kOutF32) {
-          float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
+      const bool row_ok = m < tl.row_end && ncol0 < p.N;
+      const bool full = ncol0 + kEpiCols <= p.N;
+      if (kOutF32) {
+        // FP32 out: two halves of kEpiCols / 2 columns, the first stored while
+        // the second is read, which halves the registers the drain holds; the
+        // accumulator is released after the last TMEM read
+        constexpr int kHalf = kChunks / 2;
+        float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
-          for (int j = 0; j < kEpiCols; j += 4) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[kHalf][16];
+#pragma unroll
+          for (int i = 0; i < kHalf; ++i) tmem_ld_32x32b_x16(taddr + (hf * kHalf + i) * 16, v[i]);
+          tmem_wait_ld_tied(v[0]);
+#pragma unroll
+          for (int i = 1; i < kHalf; ++i) reg_tie(v[i]);
+          if (hf == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf) * 8u);
+          }
+          if (!row_ok) continue;
+#pragma unroll
+          for (int jj = 0; jj < kHalf * 16; jj += 4) {
+            const int j = hf * kHalf * 16 + jj;
             float x[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(v[(j + e) / 16][(j + e) % 16]);
+            for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(v[(jj + e) / 16][(jj + e) % 16]);
             if (full || ncol0 + j + 4 <= p.N) {
               if (kAccum) {
                 const float4 old = *reinterpret_cast<const float4 *>(crow + j);
@@ -426,7 +473,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ncol0 + j + e < p.N) crow[j + e] = kAccum ? __fadd_rn(crow[j + e], x[e]) : x[e];
             }
           }
-        } else {
+        }
+      } else {  // BF16 out
+        uint32_t v[kChunks][16];
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) tmem_ld_32x32b_x16(taddr + i * 16, v[i]);
+        tmem_wait_ld_tied(v[0]);
+#pragma unroll
+        for (int i = 1; i < kChunks; ++i) reg_tie(v[i]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf) * 8u);
+        if (row_ok) {
           __nv_bfloat16 *crow =
               static_cast<__nv_bfloat16 *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
