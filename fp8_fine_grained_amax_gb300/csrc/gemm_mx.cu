@@ -88,6 +88,7 @@ static_assert(BN % 128 == 0 && kEpiCols % 16 == 0,
 // from waiting on the current tile's last stages
 constexpr int kRunAhead = kAccBufs == 1 ? 6 : kSfStages;
 static_assert(kAccCols + kSfStages * kSfStageCols <= kTmemCols, "TMEM budget");
+static_assert(kSfStages >= 2, "the scale ring needs TMEM columns beside the accumulators");
 constexpr int kGroupsPerStage = 4;              // one byte per K-group in a 32-bit cell
 // Scale producers: true = warps 4-7 write A exponents and warps 8-11 B
 // exponents; false = warps 4-7 write both (warps 8-11 only drain).

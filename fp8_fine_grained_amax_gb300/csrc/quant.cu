@@ -1,20 +1,25 @@
 // quant.cu -- online fine-grained E4M3 quantisers for sm_103a.
 //
-//   fp8q_quant_act     1x128 tiles (one scale per token per 128 channels)
-//   fp8q_quant_act_T   128x1 tiles along tokens, codes written transposed,
-//                      optionally also the 1x128 codes from the same read
-//   fp8q_quant_weight  128x128 blocks, optionally also the transposed codes
-//   fp8q_cast_e4m3     plain FP32 -> E4M3 conversion
+//   fp8q_quant_act      1x128 tiles (one scale per token per 128 channels)
+//   fp8q_quant_act_T    128x1 tiles along tokens, codes written transposed,
+//                       optionally also the 1x128 codes from the same read
+//   fp8q_requant_act_T  128x1 tiles from FP8-cached 1x128 activations
+//   fp8q_quant_weight   128x128 blocks, optionally also the transposed codes
+//   fp8q_quant_tensor   one scale per tensor (comparison), with a caller
+//                       workspace or (_noalloc) a fixed static scratch
+//   fp8q_cast_e4m3      plain FP32 -> E4M3 conversion
 //
 // Grouping follows dssusan.co.kr post 91437, paragraph 4 (Figure 7 (a)); the
 // scale maps each group's max-abs onto 448 ("Deepseek - Not For everyone",
 // paragraph 4); power-of-two scales follow paragraph 1 of the dssusan post.
 //
-// All four kernels are HBM-bound streaming kernels: every BF16 input byte is
-// read once with 16-byte non-caching loads, every code and scale written once.
-// The max-abs of a group is a packed 16-bit integer max over |BF16| bit
-// patterns, reduced with warp shuffles (a 1x128 group lives in 8 lanes) or
-// through shared memory (128x1 columns, 128x128 blocks).
+// They are HBM-bound streaming kernels: every input byte is read once (16-byte
+// non-caching loads or TMA tiles), every code and scale written once.  The
+// max-abs of a group is a packed 16-bit integer max over |BF16| bit patterns,
+// reduced with warp shuffles (a 1x128 group lives in 8 lanes, a 128x1 channel
+// in 4 lanes after ldmatrix.trans) or across warps (128x128 blocks).  The
+// transposed outputs leave through TMA tensor stores of swizzled shared-memory
+// tiles.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -130,12 +135,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
 }
 
 // ------------------------------------------------------------------ tiles
-// Both tile quantisers below load one 128 x 128 BF16 tile per CTA: 512
-// threads, a half-warp per 256-byte row, four rows per thread, 16-byte
-// non-caching loads.  The tile goes to shared memory as BF16 pairs, read back
-// by columns: for the column max-abs, thread (cp, tq) owns columns 2cp, 2cp+1
-// and rows 16tq..16tq+15; for the transposed codes, thread (c, q) owns column
-// c and rows 32q..32q+31 (one 32-byte sector of output).
+// The tile quantisers below (128x1, 128x1 from FP8, 128x128) work on 128 x 128
+// tiles with 512 threads (16 warps); row-wise work gives a half-warp to each
+// 256-byte row, four rows per thread.
 constexpr int kTileThreads = 512;
 
 // ------------------------------------------------------------------ 128x1
@@ -156,7 +158,7 @@ constexpr int kTileThreads = 512;
 // Channels past C are zero-filled by TMA and clipped by the TMA store.
 constexpr uint32_t kTileBytesBF16 = 128 * 128 * 2;
 constexpr uint32_t kHalfBytesBF16 = kTileBytesBF16 / 2;   // 128 tokens x 64 channels
-constexpr uint32_t kTileBytesQ = 128 * 128;                // 128 channels x 128 tokens
+constexpr uint32_t kTileBytesQ = 128 * 128;                // one 128 x 128 tile of E4M3 codes
 
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
@@ -300,8 +302,6 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 // 128-byte-swizzled FP16 tile; ldmatrix.trans reads it by channel; the
 // transposed codes leave through one TMA store.  The next tile's row scales
 // are loaded while this one is processed.
-constexpr uint32_t kTileBytesQ8 = 128 * 128;  // one tile of E4M3 codes
-
 template <bool kPow2>
 __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQT, int64_t T,
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
   __shared__ uint64_t full[2];
   __shared__ int abort_flag;
   const uint32_t raw0 = (smem_u32(dsm_raw) + 1023u) & ~1023u;  // 2 x 16 KB raw codes
-  const uint32_t tin = raw0 + 2 * kTileBytesQ8;                // 2 x 16 KB FP16 halves
+  const uint32_t tin = raw0 + 2 * kTileBytesQ;                // 2 x 16 KB FP16 halves
   const uint32_t st0 = tin + kTileBytesBF16;                   // 2 x 16 KB staged codes
 
   const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
@@ -321,8 +321,8 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
   int pending[2] = {-1, -1};
   auto issue_load = [&](int b, int64_t t) {
     const uint32_t bar = smem_u32(&full[b]);
-    mbar_arrive_expect_tx(bar, kTileBytesQ8);
-    tma_load_2d(raw0 + b * kTileBytesQ8, &tmQ, bar, static_cast<int32_t>((t % ncb) * 128),
+    mbar_arrive_expect_tx(bar, kTileBytesQ);
+    tma_load_2d(raw0 + b * kTileBytesQ, &tmQ, bar, static_cast<int32_t>((t % ncb) * 128),
                 static_cast<int32_t>((t / ncb) * 128));
   };
   auto row_scale = [&](int64_t t) {  // threads < 128: this tile's scale of token row tid
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
       uint2 q8;
       asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                    : "=r"(q8.x), "=r"(q8.y)
-                   : "r"(raw0 + buf * kTileBytesQ8 + r * 128u + 8u * l16));
+                   : "r"(raw0 + buf * kTileBytesQ + r * 128u + 8u * l16));
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
                        tin + (l16 >> 3) * kHalfBytesBF16 + swz128(r, static_cast<uint32_t>(l16 & 7))),
                    "r"(decode_e4m3x2(static_cast<uint16_t>(q8.x & 0xFFFF))),
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
 
     if (tid == 0) bulk_wait_group_read<1>();  // stage `buf`: its store two tiles ago has read it
     __syncthreads();  // every thread is done with the FP16 tile and row scales
-    const uint32_t stg = st0 + buf * kTileBytesQ8;
+    const uint32_t stg = st0 + buf * kTileBytesQ;
 #pragma unroll
     for (int m = 0; m < 16; ++m)
       st_shared_u16(stg + swz128(static_cast<uint32_t>(cw), static_cast<uint32_t>(m >> 1)) +
@@ -654,7 +654,7 @@ fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX,
   return launch_status();
 }
 
-constexpr size_t kRequantSmem = 2 * kTileBytesQ8 + kTileBytesBF16 + 2 * kTileBytesQ8 + 1024;
+constexpr size_t kRequantSmem = 2 * kTileBytesQ + kTileBytesBF16 + 2 * kTileBytesQ + 1024;
 constexpr int kRequantCtasPerSm = 2;
 
 template <bool kPow2>
