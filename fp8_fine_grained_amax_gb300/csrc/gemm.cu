@@ -21,9 +21,11 @@
 //   warps 4-11  epilogue: tcgen05.ld the partial (each thread one row, 128
 //               columns, 16 at a time), acc += P * sa(m,kb) * sb(n,kb) in FP32
 //               registers with packed two-lane FMAs (fma.rn.f32x2), release the
-//               TMEM buffer; after the last group, store C as FP32 or
-//               round-to-nearest-even BF16.  The scales of group kb+1 are
-//               loaded while group kb is folded.
+//               TMEM buffer; after the last group, round C to BF16 (nearest
+//               even) or keep FP32, stage it in shared memory 32 rows x 32
+//               bytes at a time and write it with TMA tensor stores, which
+//               drain while the next tile is folded.  The scales of group
+//               kb+1 are loaded while group kb is folded.
 //
 // Registers: the kernel is built for 384 threads at 168 registers each (the
 // register file of each SM sub-partition holds three warps at 168).  The
@@ -73,7 +75,7 @@ constexpr int kGroupM = 16;   // L2 rasterisation band (m-tiles) for the dense G
 constexpr int kMaxGroups = 1024;
 constexpr uint64_t kDrainNs = 1000000000ull;  // 1 s for draining after an abort
 constexpr int kMaxStages = 6;
-constexpr bool kGroupedPair = false;  // tile shape of the grouped (MoE) GEMM
+constexpr bool kGroupedPair = true;   // tile shape of the grouped (MoE) GEMM
 constexpr bool kDensePair = true;    // tile shape of the dense GEMMs
 
 // Two shapes of the same pipeline:
@@ -131,7 +133,7 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-// Shared-memory control block, after the operand ring (1024-byte aligned).
+// Shared-memory control block, after the operand ring and the output staging.
 struct alignas(8) SmemCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
@@ -145,9 +147,15 @@ struct alignas(8) SmemCtl {
   alignas(16) float sb_warp[kEpiWarps][2][kEpiCols];
 };
 
+// Output staging: each epilogue warp owns two 1 KB buffers of 32 rows x 32
+// bytes (16 BF16 or 8 FP32 columns), written in the 32-byte swizzle and
+// drained to global memory by TMA tensor stores.
+constexpr uint32_t kStageCBuf = 32 * 32;
+constexpr uint32_t kStageCBytes = kEpiWarps * 2 * kStageCBuf;
+
 __host__ __device__ constexpr size_t smem_bytes(bool grouped, bool pair) {
   return 1024 /* alignment slack */ + (pair ? Cfg<true>::kTileBytes : Cfg<false>::kTileBytes) +
-         sizeof(SmemCtl) + (grouped ? 3 * (kMaxGroups + 1) * sizeof(int) : 0);
+         kStageCBytes + sizeof(SmemCtl) + (grouped ? 2 * (kMaxGroups + 1) * sizeof(int) : 0);
 }
 
 struct Tile {
@@ -158,11 +166,11 @@ struct Tile {
   int g;        // expert (grouped) or 0
 };
 
-// Grouped tables in shared memory: s_lo[g] / s_hi[g] = clamped row range of
+// Grouped tables in shared memory: s_lo[g] .. s_lo[g + 1] = clamped row range of
 // expert g, s_pre[g] = number of m-tiles of experts before g (s_pre[G] = all).
 template <bool kGrouped, int kTileM>
 __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_lo,
-                                        const int *s_hi, const int *s_pre) {
+                                        const int *s_pre) {
   Tile r;
   if (!kGrouped) {
     const int band_tiles = kGroupM * p.tiles_n;
@@ -188,7 +196,7 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_l
     const int local = t - s_pre[g] * p.tiles_n;
     const int mt = local % mtiles, nt = local / mtiles;
     r.a_row = s_lo[g] + mt * kTileM;
-    r.row_end = s_hi[g];
+    r.row_end = s_lo[g + 1];
     r.n0 = nt * BN;
     r.b_row = g * p.N + r.n0;
     r.g = g;
@@ -199,17 +207,17 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_l
 template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8q_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmArgs p) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
   using C = Cfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::kStages * C::kABytes;
-  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + C::kTileBytes);
+  uint8_t *sC = smem + C::kTileBytes;  // output staging (1024-byte aligned)
+  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(sC + kStageCBytes);
   int *s_lo = reinterpret_cast<int *>(ctl + 1);  // grouped only (see tile_of)
-  int *s_hi = s_lo + (kMaxGroups + 1);
-  int *s_prefix = s_hi + (kMaxGroups + 1);
+  int *s_prefix = s_lo + (kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int *abort_flag = &ctl->abort_flag;
@@ -234,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     if (kPair) tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -252,17 +261,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (threadIdx.x == 0) {
       // ranges never overlap: an expert starts no earlier than the previous
-      // one ended, and a decreasing offset makes it empty
+      // one ended, and a decreasing offset makes it empty; expert g then
+      // owns rows s_lo[g] .. s_lo[g + 1]
       int acc = 0, prev_hi = 0;
       for (int g = 0; g < p.G; ++g) {
         const int lo = max(s_lo[g], prev_hi);
         const int hi = max(lo, s_lo[g + 1]);
         s_lo[g] = lo;
-        s_hi[g] = hi;
         s_prefix[g] = acc;
         acc += (hi - lo + C::kTileM - 1) / C::kTileM;
         prev_hi = hi;
       }
+      s_lo[p.G] = prev_hi;
       s_prefix[p.G] = acc;
     }
     __syncthreads();
@@ -290,9 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tb = 0;
     uint32_t tphase = 0;
     uint32_t sb_iter = 0;
+    uint32_t st_count = 0;  // tensor stores issued by this warp (staging buffer parity)
     bool ok = true;
     for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
-      const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_hi, s_prefix);
+      const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_prefix);
       const int m = tl.a_row + row_in_tile;
       const bool row_in = m < p.M;
       const int ncol0 = tl.n0 + col_base;
@@ -405,13 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 
-      // ---- store this thread's row segment (kEpiCols columns of row m)
-      if (m < tl.row_end && ncol0 < p.N) {
+      // ---- store this warp's 32 rows x kEpiCols columns
+      // Whole 32-byte column chunks go out as TMA tensor stores of a staged
+      // 32 x 32-byte box (asynchronous: the next tile's fold starts while they
+      // drain).  Thread-level stores remain for C += (read-modify-write), for
+      // per-column B scales, for a grouped warp whose rows cross the expert's
+      // end (the tensor map only clips at M), and for a last chunk that ends
+      // inside a 16-byte unit (tensor stores clip the inner dimension at
+      // 16-byte granularity).
+      constexpr int kEsz = kOutF32 ? 4 : 2;
+      constexpr int kChunkCols = 32 / kEsz;
+      const int wrow0 = tl.a_row + row_in_tile - lane;
+      // (per-column scales: the heavier fold leaves no registers for the
+      // staging path without spills, and those cost more than it saves)
+      constexpr bool kTmaStore = !kAccum && kBScale != FP8Q_BSCALE_ROW;
+      const bool rows_tma = kTmaStore && (!kGrouped || wrow0 + 32 <= tl.row_end);
+      const bool n_exact = (p.N * kEsz) % 16 == 0;
+      auto store_direct = [&](int j0, int j1) {  // columns [j0, j1) of the thread's segment
+        if (!(m < tl.row_end)) return;
         const bool full = ncol0 + kEpiCols <= p.N;
         if (kOutF32) {
           float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
           for (int j = 0; j < kEpiCols; j += 4) {
+            if (j < j0 || j >= j1 || (!full && ncol0 + j >= p.N)) continue;
             const float2 lo = unpack_f32x2(acc[j / 2]), hi = unpack_f32x2(acc[j / 2 + 1]);
             float v[4] = {lo.x, lo.y, hi.x, hi.y};
             if (full || ncol0 + j + 4 <= p.N) {
@@ -433,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               static_cast<__nv_bfloat16 *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
           for (int j = 0; j < kEpiCols; j += 8) {
+            if (j < j0 || j >= j1 || (!full && ncol0 + j >= p.N)) continue;
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -450,8 +479,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      };
+      if (ncol0 < p.N && wrow0 < tl.row_end) {
+        int d0 = 0, d1 = rows_tma ? 0 : kEpiCols;  // columns left to thread-level stores
+        if (rows_tma) {
+#pragma unroll
+          for (int j = 0; j < kEpiCols; j += kChunkCols) {
+            const int x = ncol0 + j;
+            if (x >= p.N) break;
+            if (x + kChunkCols > p.N && !n_exact) {
+              d0 = j;
+              d1 = j + kChunkCols;
+              break;
+            }
+            // this row's 32 bytes as two 16-byte units, unit u at u ^ bit 2 of
+            // the row (the tensor map's 32-byte swizzle)
+            uint4 u[2];
+            if (kOutF32) {
+              u[0] = make_uint4(static_cast<uint32_t>(acc[j / 2]),
+                                static_cast<uint32_t>(acc[j / 2] >> 32),
+                                static_cast<uint32_t>(acc[j / 2 + 1]),
+                                static_cast<uint32_t>(acc[j / 2 + 1] >> 32));
+              u[1] = make_uint4(static_cast<uint32_t>(acc[j / 2 + 2]),
+                                static_cast<uint32_t>(acc[j / 2 + 2] >> 32),
+                                static_cast<uint32_t>(acc[j / 2 + 3]),
+                                static_cast<uint32_t>(acc[j / 2 + 3] >> 32));
+            } else {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float2 v = unpack_f32x2(acc[j / 2 + e]);
+                __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+                w[e] = *reinterpret_cast<uint32_t *>(&h);
+              }
+              u[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              u[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            const uint32_t buf = smem_u32(sC) + (2 * ew + (st_count & 1)) * kStageCBuf;
+            // the store that last read this buffer (two stores ago) must be done
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            const uint32_t sw = (lane >> 2) & 1;
+            st_shared_v4(buf + lane * 32 + 16 * sw, u[0]);
+            st_shared_v4(buf + lane * 32 + 16 * (sw ^ 1), u[1]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, buf, x, wrow0);
+              bulk_commit_group();
+            }
+            ++st_count;
+          }
+        }
+        if (d1 > d0) store_direct(d0, d1);
       }
     }
+    // every tensor store of this warp has written global memory
+    if (lane == 0) bulk_wait_group_all();
     // teardown (epilogue side): TMEM reads are complete
     __syncwarp();
     tc_fence_before();
@@ -469,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0, armed_phase = 0;  // per-stage bit masks
       bool ok = true;
       for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
-        const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_hi, s_prefix);
+        const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_prefix);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1, abort_flag, &g_status,
                                  p.timeout_ns, FP8Q_ERR_TIMEOUT)) {
@@ -600,12 +684,21 @@ bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// C [rows][cols] (BF16 or FP32) with row pitch ld elements, box 32 rows x 32
+// bytes in the 32-byte swizzle: the epilogue's staged output chunks.
+bool make_tmap_c(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, uint64_t ld,
+                 bool f32) {
+  return make_tmap_2d(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      base, rows, cols, ld * (f32 ? 4 : 2), f32 ? 8 : 16, 32,
+                      CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
 // Launch one instantiation.  `work_tiles` is the number of output tiles (an
 // upper bound for the grouped GEMM); the grid is persistent: one CTA (or one
 // CTA pair) per SM that can hold one, never more than there are tiles.
 template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false>
-fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
-                   int64_t work_tiles, cudaStream_t s) {
+fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                   const GemmArgs &args, int64_t work_tiles, cudaStream_t s) {
   auto kern = fp8q_gemm_kernel<kBScale, kOutF32, kGrouped, kPair, kAccum>;
   const size_t smem = smem_bytes(kGrouped, kPair);
   static int max_units[kMaxDevices] = {};  // co-resident CTAs (or CTA pairs) per device
@@ -646,7 +739,7 @@ fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs 
   }
   const int64_t units = work_tiles < max_units[dev] ? work_tiles : max_units[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(units * (kPair ? 2 : 1)), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, args) != cudaSuccess) return FP8Q_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args) != cudaSuccess) return FP8Q_ERR_CUDA;
   return launch_status();
 }
 
@@ -654,34 +747,35 @@ fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs 
 // or single CTAs (128 x 256 tiles) for the dense and grouped GEMMs.
 // C (FP32) += result: dense GEMMs only (gradient accumulation).
 fp8q_status dispatch_accumulate(int bkind, const CUtensorMap &ta, const CUtensorMap &tb,
-                                const GemmArgs &a, int64_t tiles, cudaStream_t s) {
+                                const CUtensorMap &tc, const GemmArgs &a, int64_t tiles,
+                                cudaStream_t s) {
   switch (bkind) {
     case FP8Q_BSCALE_BLOCK:
-      return launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair, true>(ta, tb, a, tiles, s);
+      return launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair, true>(ta, tb, tc, a, tiles, s);
     case FP8Q_BSCALE_BLOCK_T:
-      return launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair, true>(ta, tb, a, tiles, s);
+      return launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair, true>(ta, tb, tc, a, tiles, s);
     default:
-      return launch<FP8Q_BSCALE_ROW, true, false, kDensePair, true>(ta, tb, a, tiles, s);
+      return launch<FP8Q_BSCALE_ROW, true, false, kDensePair, true>(ta, tb, tc, a, tiles, s);
   }
 }
 
 template <bool kGrouped>
 fp8q_status dispatch(int bkind, bool f32, const CUtensorMap &ta, const CUtensorMap &tb,
-                     const GemmArgs &a, int64_t tiles, cudaStream_t s) {
+                     const CUtensorMap &tc, const GemmArgs &a, int64_t tiles, cudaStream_t s) {
   if (kGrouped) {
-    return f32 ? launch<FP8Q_BSCALE_BLOCK, true, true, kGroupedPair>(ta, tb, a, tiles, s)
-               : launch<FP8Q_BSCALE_BLOCK, false, true, kGroupedPair>(ta, tb, a, tiles, s);
+    return f32 ? launch<FP8Q_BSCALE_BLOCK, true, true, kGroupedPair>(ta, tb, tc, a, tiles, s)
+               : launch<FP8Q_BSCALE_BLOCK, false, true, kGroupedPair>(ta, tb, tc, a, tiles, s);
   }
   switch (bkind) {
     case FP8Q_BSCALE_BLOCK:
-      return f32 ? launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair>(ta, tb, a, tiles, s)
-                 : launch<FP8Q_BSCALE_BLOCK, false, false, kDensePair>(ta, tb, a, tiles, s);
+      return f32 ? launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
+                 : launch<FP8Q_BSCALE_BLOCK, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
     case FP8Q_BSCALE_BLOCK_T:
-      return f32 ? launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair>(ta, tb, a, tiles, s)
-                 : launch<FP8Q_BSCALE_BLOCK_T, false, false, kDensePair>(ta, tb, a, tiles, s);
+      return f32 ? launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
+                 : launch<FP8Q_BSCALE_BLOCK_T, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
     default:
-      return f32 ? launch<FP8Q_BSCALE_ROW, true, false, kDensePair>(ta, tb, a, tiles, s)
-                 : launch<FP8Q_BSCALE_ROW, false, false, kDensePair>(ta, tb, a, tiles, s);
+      return f32 ? launch<FP8Q_BSCALE_ROW, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
+                 : launch<FP8Q_BSCALE_ROW, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
   }
 }
 
@@ -733,9 +827,11 @@ static fp8q_status gemm_entry(const void *a, int64_t lda, const float *sa, int64
   // Each CTA of a pair loads 128 rows of A and 128 rows (half a tile) of B.
   const void *abase = K > 0 ? a : c;
   const void *bbase = K > 0 ? b : c;
+  CUtensorMap tc;
   if (!make_tmap_u8(&ta, abase, K > 0 ? M : 1, K > 0 ? K : 128, K > 0 ? lda : 128, BM) ||
       !make_tmap_u8(&tb, bbase, K > 0 ? N : 1, K > 0 ? K : 128, K > 0 ? ldb : 128,
-                    kDensePair ? BN / 2 : BN))
+                    kDensePair ? BN / 2 : BN) ||
+      !make_tmap_c(&tc, c, M, N, ldc, out_dtype == FP8Q_OUT_FP32))
     return FP8Q_ERR_CUDA;
   GemmArgs args{};
   args.sa = sa;
@@ -755,8 +851,9 @@ static fp8q_status gemm_entry(const void *a, int64_t lda, const float *sa, int64
   const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
   if (tiles >= (1ll << 31)) return FP8Q_ERR_SHAPE;
   if (accumulate)
-    return dispatch_accumulate(bscale_kind, ta, tb, args, tiles, static_cast<cudaStream_t>(stream));
-  return dispatch<false>(bscale_kind, out_dtype == FP8Q_OUT_FP32, ta, tb, args, tiles,
+    return dispatch_accumulate(bscale_kind, ta, tb, tc, args, tiles,
+                               static_cast<cudaStream_t>(stream));
+  return dispatch<false>(bscale_kind, out_dtype == FP8Q_OUT_FP32, ta, tb, tc, args, tiles,
                          static_cast<cudaStream_t>(stream));
 }
 
@@ -798,9 +895,11 @@ extern "C" fp8q_status fp8q_grouped_gemm(const void *a, int64_t lda, const float
   CUtensorMap ta, tb;
   const void *abase = K > 0 ? a : c;
   const void *bbase = K > 0 ? b : c;
+  CUtensorMap tc;
   if (!make_tmap_u8(&ta, abase, K > 0 ? M : 1, K > 0 ? K : 128, K > 0 ? lda : 128, BM) ||
       !make_tmap_u8(&tb, bbase, K > 0 ? static_cast<uint64_t>(G) * N : 1, K > 0 ? K : 128,
-                    K > 0 ? ldb : 128, kGroupedPair ? BN / 2 : BN))
+                    K > 0 ? ldb : 128, kGroupedPair ? BN / 2 : BN) ||
+      !make_tmap_c(&tc, c, M, N, ldc, out_dtype == FP8Q_OUT_FP32))
     return FP8Q_ERR_CUDA;
   GemmArgs args{};
   args.sa = sa;
@@ -820,7 +919,7 @@ extern "C" fp8q_status fp8q_grouped_gemm(const void *a, int64_t lda, const float
   // upper bound on tiles: each expert adds at most one partial m-tile
   const int64_t bound = (static_cast<int64_t>(args.tiles_m) + G) * args.tiles_n;
   if (bound >= (1ll << 31)) return FP8Q_ERR_SHAPE;
-  return dispatch<true>(FP8Q_BSCALE_BLOCK, out_dtype == FP8Q_OUT_FP32, ta, tb, args, bound,
+  return dispatch<true>(FP8Q_BSCALE_BLOCK, out_dtype == FP8Q_OUT_FP32, ta, tb, tc, args, bound,
                         static_cast<cudaStream_t>(stream));
 }
 
