@@ -300,7 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tb = 0;
     uint32_t tphase = 0;
     uint32_t sb_iter = 0;
-    uint32_t st_count = 0;  // tensor stores issued by this warp (staging buffer parity)
     bool ok = true;
     for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
       const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_prefix);
@@ -417,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---- store this warp's 32 rows x kEpiCols columns
-      // Whole 32-byte column chunks go out as TMA tensor stores of a staged
-      // 32 x 32-byte box (asynchronous: the next tile's fold starts while they
-      // drain).  Thread-level stores remain for C += (read-modify-write), for
+      // Whole 32-byte column chunks go out as TMA tensor stores of staged
+      // 32 x 32-byte boxes, two per round (asynchronous: the next tile's fold
+      // starts while they drain).  Thread-level stores remain for C += (read-modify-write), for
       // per-column B scales, for a grouped warp whose rows cross the expert's
       // end (the tensor map only clips at M), and for a last chunk that ends
       // inside a 16-byte unit (tensor stores clip the inner dimension at
@@ -483,18 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ncol0 < p.N && wrow0 < tl.row_end) {
         int d0 = 0, d1 = rows_tma ? 0 : kEpiCols;  // columns left to thread-level stores
         if (rows_tma) {
-#pragma unroll
-          for (int j = 0; j < kEpiCols; j += kChunkCols) {
-            const int x = ncol0 + j;
-            if (x >= p.N) break;
-            if (x + kChunkCols > p.N && !n_exact) {
-              d0 = j;
-              d1 = j + kChunkCols;
-              break;
-            }
-            // this row's 32 bytes as two 16-byte units, unit u at u ^ bit 2 of
-            // the row (the tensor map's 32-byte swizzle)
-            uint4 u[2];
+          // leading chunks that go out as tensor stores; a ragged last chunk
+          // (ending inside a 16-byte unit) is left to thread-level stores
+          const int cols = min(kEpiCols, p.N - ncol0);
+          const int n_chunks = n_exact ? (cols + kChunkCols - 1) / kChunkCols : cols / kChunkCols;
+          if (n_chunks * kChunkCols < cols) {
+            d0 = n_chunks * kChunkCols;
+            d1 = d0 + kChunkCols;
+          }
+          auto pack = [&](int j, uint4 (&u)[2]) {
             if (kOutF32) {
               u[0] = make_uint4(static_cast<uint32_t>(acc[j / 2]),
                                 static_cast<uint32_t>(acc[j / 2] >> 32),
@@ -515,20 +511,33 @@ __global__ void __launch_bounds__(kThreads, 1)
               u[0] = make_uint4(w[0], w[1], w[2], w[3]);
               u[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
-            const uint32_t buf = smem_u32(sC) + (2 * ew + (st_count & 1)) * kStageCBuf;
-            // the store that last read this buffer (two stores ago) must be done
-            if (lane == 0) bulk_wait_group_read<1>();
+          };
+          const uint32_t buf0 = smem_u32(sC) + 2 * ew * kStageCBuf;
+          const uint32_t sw = (lane >> 2) & 1;
+#pragma unroll
+          for (int j = 0; j < kEpiCols; j += 2 * kChunkCols) {
+            const int c = j / kChunkCols;
+            if (c >= n_chunks) break;
+            const bool two = c + 1 < n_chunks;
+            uint4 u0[2], u1[2];
+            pack(j, u0);
+            if (two) pack(j + kChunkCols, u1);
+            // both buffers' previous stores must have read them
+            if (lane == 0) bulk_wait_group_read<0>();
             __syncwarp();
-            const uint32_t sw = (lane >> 2) & 1;
-            st_shared_v4(buf + lane * 32 + 16 * sw, u[0]);
-            st_shared_v4(buf + lane * 32 + 16 * (sw ^ 1), u[1]);
+            st_shared_v4(buf0 + lane * 32 + 16 * sw, u0[0]);
+            st_shared_v4(buf0 + lane * 32 + 16 * (sw ^ 1), u0[1]);
+            if (two) {
+              st_shared_v4(buf0 + kStageCBuf + lane * 32 + 16 * sw, u1[0]);
+              st_shared_v4(buf0 + kStageCBuf + lane * 32 + 16 * (sw ^ 1), u1[1]);
+            }
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmC, buf, x, wrow0);
+              tma_store_2d(&tmC, buf0, ncol0 + j, wrow0);
+              if (two) tma_store_2d(&tmC, buf0 + kStageCBuf, ncol0 + j + kChunkCols, wrow0);
               bulk_commit_group();
             }
-            ++st_count;
           }
         }
         if (d1 > d0) store_direct(d0, d1);
