@@ -22,10 +22,10 @@
 //               columns, 16 at a time), acc += P * sa(m,kb) * sb(n,kb) in FP32
 //               registers with packed two-lane FMAs (fma.rn.f32x2), release the
 //               TMEM buffer; after the last group, round C to BF16 (nearest
-//               even) or keep FP32, stage it in shared memory 32 rows x 32
-//               bytes at a time and write it with TMA tensor stores, which
-//               drain while the next tile is folded.  The scales of group
-//               kb+1 are loaded while group kb is folded.
+//               even) or keep FP32 and write it out through a per-warp
+//               shared-memory buffer: coalesced 16-byte stores (dense) or
+//               TMA tensor stores (grouped).  The scales of group kb+1 are
+//               loaded while group kb is folded.
 //
 // Registers: the kernel is built for 384 threads at 168 registers each (the
 // register file of each SM sub-partition holds three warps at 168).  The
@@ -416,20 +416,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---- store this warp's 32 rows x kEpiCols columns
-      // Whole 32-byte column chunks go out as TMA tensor stores of staged
-      // 32 x 32-byte boxes, two per round (asynchronous: the next tile's fold
-      // starts while they drain).  Thread-level stores remain for C += (read-modify-write), for
-      // per-column B scales, for a grouped warp whose rows cross the expert's
-      // end (the tensor map only clips at M), and for a last chunk that ends
-      // inside a 16-byte unit (tensor stores clip the inner dimension at
-      // 16-byte granularity).
+      // Dense tiles: 64 bytes of each row at a time go through a 2 KB
+      // shared-memory buffer (64-byte swizzle) and leave as 16-byte stores,
+      // four lanes per row, so one instruction writes eight whole 64-byte row
+      // segments (the thread-per-row layout would touch 32 lines).
+      // Grouped tiles: 32-byte column chunks staged in two 1 KB buffers
+      // (32-byte swizzle) leave as TMA tensor stores, two per round, which
+      // drain while the next tile is folded.  Thread-level stores remain for
+      // C += (read-modify-write), for per-column B scales, for a grouped warp
+      // whose rows cross the expert's end (the tensor map only clips at M),
+      // and for a last tensor-store chunk that ends inside a 16-byte unit
+      // (tensor stores clip the inner dimension at 16-byte granularity).
       constexpr int kEsz = kOutF32 ? 4 : 2;
       constexpr int kChunkCols = 32 / kEsz;
       const int wrow0 = tl.a_row + row_in_tile - lane;
       // (per-column scales: the heavier fold leaves no registers for the
-      // staging path without spills, and those cost more than it saves)
-      constexpr bool kTmaStore = !kAccum && kBScale != FP8Q_BSCALE_ROW;
-      const bool rows_tma = kTmaStore && (!kGrouped || wrow0 + 32 <= tl.row_end);
+      // staging paths without spills, and those cost more than they save)
+      constexpr bool kStaged = !kAccum && kBScale != FP8Q_BSCALE_ROW;
+      const bool staged = kStaged && (!kGrouped || wrow0 + 32 <= tl.row_end);
       const bool n_exact = (p.N * kEsz) % 16 == 0;
       auto store_direct = [&](int j0, int j1) {  // columns [j0, j1) of the thread's segment
         if (!(m < tl.row_end)) return;
@@ -480,8 +484,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       if (ncol0 < p.N && wrow0 < tl.row_end) {
-        int d0 = 0, d1 = rows_tma ? 0 : kEpiCols;  // columns left to thread-level stores
-        if (rows_tma) {
+        int d0 = 0, d1 = staged ? 0 : kEpiCols;  // columns left to thread-level stores
+        if (kStaged && !kGrouped) {
+          // coalesced: each warp transposes its rows through shared memory
+          constexpr int kUnitCols = 16 / kEsz;  // columns per 16-byte unit
+          constexpr int kRowCols = 64 / kEsz;   // columns per staged 64-byte row
+          const uint32_t buf = smem_u32(sC) + ew * (2 * kStageCBuf);
+          const uint32_t swz = (lane >> 1) & 3;
+          const int rsub = lane >> 2, unit = lane & 3;
+#pragma unroll
+          for (int j = 0; j < kEpiCols; j += kRowCols) {
+            if (ncol0 + j >= p.N) break;
+            uint4 u[4];
+            if (kOutF32) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                u[q] = make_uint4(static_cast<uint32_t>(acc[j / 2 + 2 * q]),
+                                  static_cast<uint32_t>(acc[j / 2 + 2 * q] >> 32),
+                                  static_cast<uint32_t>(acc[j / 2 + 2 * q + 1]),
+                                  static_cast<uint32_t>(acc[j / 2 + 2 * q + 1] >> 32));
+            } else {
+              uint32_t w[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float2 v = unpack_f32x2(acc[j / 2 + e]);
+                __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+                w[e] = *reinterpret_cast<uint32_t *>(&h);
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) u[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            }
+            __syncwarp();  // the previous chunk has been read back
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_shared_v4(buf + lane * 64 + 16 * (q ^ swz), u[q]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = rsub + 8 * i;
+              const uint4 v = ld_shared_v4(buf + r * 64 + 16 * (unit ^ ((r >> 1) & 3)));
+              const int row = wrow0 + r;
+              const int col = ncol0 + j + unit * kUnitCols;
+              if (row < tl.row_end && col < p.N) {
+                uint8_t *dst = static_cast<uint8_t *>(p.c) +
+                               (static_cast<int64_t>(row) * p.ldc + col) * kEsz;
+                if (col + kUnitCols <= p.N) {
+                  *reinterpret_cast<uint4 *>(dst) = v;
+                } else {
+                  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                  for (int e = 0; e < kUnitCols && col + e < p.N; ++e) {
+                    if (kOutF32) reinterpret_cast<uint32_t *>(dst)[e] = wv[e];
+                    else reinterpret_cast<uint16_t *>(dst)[e] = static_cast<uint16_t>(wv[e >> 1] >> (16 * (e & 1)));
+                  }
+                }
+              }
+            }
+          }
+        }
+        if (kStaged && kGrouped && wrow0 + 32 <= tl.row_end) {
           // leading chunks that go out as tensor stores; a ragged last chunk
           // (ending inside a 16-byte unit) is left to thread-level stores
           const int cols = min(kEpiCols, p.N - ncol0);
