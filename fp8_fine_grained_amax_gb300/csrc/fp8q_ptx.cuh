@@ -143,6 +143,56 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+// One warp writes a block of 32 rows x 64 bytes of a row-major matrix C, row r
+// of the block held by lane r as four 16-byte units u[0..3], through a 2 KB
+// shared-memory buffer `buf`: the units go in under a 64-byte XOR swizzle
+// (unit q of row r at q ^ ((r >> 1) & 3), conflict-free) and come back four
+// lanes per row, so each 16-byte global store writes eight whole 64-byte row
+// segments instead of 32 scattered pieces.  The block starts at (row0, col0);
+// rows >= row_end and columns >= n are left alone.  kEsz: element size (2 or
+// 4); kAccum (FP32 only): C += values, one FP32 addition per element.
+template <int kEsz, bool kAccum>
+__device__ __forceinline__ void warp_store_block64(uint32_t buf, const uint4 (&u)[4], void *c,
+                                                   int64_t ldc, int row0, int row_end, int col0,
+                                                   int n, int lane) {
+  static_assert(!kAccum || kEsz == 4, "C += is FP32 only");
+  constexpr int kUnitCols = 16 / kEsz;
+  __syncwarp();  // the buffer's previous block has been read back
+  const uint32_t swz = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) st_shared_v4(buf + lane * 64 + 16 * (q ^ swz), u[q]);
+  __syncwarp();
+  const int unit = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = (lane >> 2) + 8 * i;
+    uint4 v = ld_shared_v4(buf + r * 64 + 16 * (unit ^ ((r >> 1) & 3)));
+    const int row = row0 + r, col = col0 + unit * kUnitCols;
+    if (row >= row_end || col >= n) continue;
+    uint8_t *dst = static_cast<uint8_t *>(c) + (static_cast<int64_t>(row) * ldc + col) * kEsz;
+    if (col + kUnitCols <= n) {
+      if (kAccum) {
+        const float4 old = *reinterpret_cast<const float4 *>(dst);
+        v.x = __float_as_uint(__fadd_rn(old.x, __uint_as_float(v.x)));
+        v.y = __float_as_uint(__fadd_rn(old.y, __uint_as_float(v.y)));
+        v.z = __float_as_uint(__fadd_rn(old.z, __uint_as_float(v.z)));
+        v.w = __float_as_uint(__fadd_rn(old.w, __uint_as_float(v.w)));
+      }
+      *reinterpret_cast<uint4 *>(dst) = v;
+    } else {
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int e = 0; e < kUnitCols && col + e < n; ++e) {
+        if (kEsz == 4) {
+          float *d = reinterpret_cast<float *>(dst) + e;
+          *d = kAccum ? __fadd_rn(*d, __uint_as_float(w[e])) : __uint_as_float(w[e]);
+        } else {
+          reinterpret_cast<uint16_t *>(dst)[e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+        }
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

@@ -486,12 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ncol0 < p.N && wrow0 < tl.row_end) {
         int d0 = 0, d1 = staged ? 0 : kEpiCols;  // columns left to thread-level stores
         if (kStaged && !kGrouped) {
-          // coalesced: each warp transposes its rows through shared memory
-          constexpr int kUnitCols = 16 / kEsz;  // columns per 16-byte unit
-          constexpr int kRowCols = 64 / kEsz;   // columns per staged 64-byte row
+          // coalesced: 64 bytes of each row at a time through the warp's 2 KB
+          constexpr int kRowCols = 64 / kEsz;
           const uint32_t buf = smem_u32(sC) + ew * (2 * kStageCBuf);
-          const uint32_t swz = (lane >> 1) & 3;
-          const int rsub = lane >> 2, unit = lane & 3;
 #pragma unroll
           for (int j = 0; j < kEpiCols; j += kRowCols) {
             if (ncol0 + j >= p.N) break;
@@ -512,32 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w[e] = *reinterpret_cast<uint32_t *>(&h);
               }
 #pragma unroll
-              for (int q = 0; q < 4; ++q) u[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+              for (int q = 0; q < 4; ++q)
+                u[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
-            __syncwarp();  // the previous chunk has been read back
-#pragma unroll
-            for (int q = 0; q < 4; ++q) st_shared_v4(buf + lane * 64 + 16 * (q ^ swz), u[q]);
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = rsub + 8 * i;
-              const uint4 v = ld_shared_v4(buf + r * 64 + 16 * (unit ^ ((r >> 1) & 3)));
-              const int row = wrow0 + r;
-              const int col = ncol0 + j + unit * kUnitCols;
-              if (row < tl.row_end && col < p.N) {
-                uint8_t *dst = static_cast<uint8_t *>(p.c) +
-                               (static_cast<int64_t>(row) * p.ldc + col) * kEsz;
-                if (col + kUnitCols <= p.N) {
-                  *reinterpret_cast<uint4 *>(dst) = v;
-                } else {
-                  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                  for (int e = 0; e < kUnitCols && col + e < p.N; ++e) {
-                    if (kOutF32) reinterpret_cast<uint32_t *>(dst)[e] = wv[e];
-                    else reinterpret_cast<uint16_t *>(dst)[e] = static_cast<uint16_t>(wv[e >> 1] >> (16 * (e & 1)));
-                  }
-                }
-              }
-            }
+            warp_store_block64<kEsz, false>(buf, u, p.c, p.ldc, wrow0, tl.row_end, ncol0 + j,
+                                            p.N, lane);
           }
         }
         if (kStaged && kGrouped && wrow0 + 32 <= tl.row_end) {

@@ -30,7 +30,9 @@
 //               +q for lane quarter q), warps 8-11 the B exponents of the
 //               tile's BN columns (columns +8.., the same in every lane
 //               quarter).  At the end of a tile they read its accumulator
-//               (each thread BN/2 columns of its row), release it and store C.
+//               (each thread BN/2 columns of its row), release it and store C
+//               through a 2 KB shared-memory buffer per warp, 64 bytes of
+//               each row at a time, as coalesced 16-byte stores.
 //
 // Shipped shape: BN = 256 with one accumulator (columns 0-255) and 16 scale
 // stages (columns 256-511).  The epilogue writes scale stages up to 6 ahead
@@ -126,7 +128,10 @@ struct alignas(8) MxCtl {
 
 constexpr int kMaxGroups = 1024;
 constexpr size_t kGroupTables = 3 * (kMaxGroups + 1) * sizeof(int);
-constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(MxCtl);
+// Output staging: 2 KB per epilogue warp (32 rows x 64 bytes) for coalesced
+// stores of the drained accumulator.
+constexpr size_t kStageBytes = kEpiWarps * 2048;
+constexpr size_t kSmemBytes = 1024 + kRingBytes + kStageBytes + sizeof(MxCtl);
 
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -202,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + kStages * kABytes;
-  MxCtl *ctl = reinterpret_cast<MxCtl *>(smem + kRingBytes);
+  uint8_t *sC = smem + kRingBytes;  // output staging (1024-byte aligned)
+  MxCtl *ctl = reinterpret_cast<MxCtl *>(sC + kStageBytes);
   int *s_lo = reinterpret_cast<int *>(ctl + 1);  // grouped only (see mx_tile_of)
   int *s_hi = s_lo + (kMaxGroups + 1);
   int *s_pre = s_hi + (kMaxGroups + 1);
@@ -418,28 +424,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    // Read tile t's accumulator (buffer buf), release it, store C.
-    auto drain = [&](int t, int buf) -> bool {
-      const bool got = mbar_wait_bounded(smem_u32(&ctl->tfull[buf]), (tphase >> buf) & 1u,
+    // Read tile t's accumulator (buffer buf_acc), release it, store C through the
+    // warp's shared-memory buffer (coalesced 16-byte stores).
+    auto drain = [&](int t, int buf_acc) -> bool {
+      const bool got = mbar_wait_bounded(smem_u32(&ctl->tfull[buf_acc]), (tphase >> buf_acc) & 1u,
                                          abort_flag, &g_mx_status, p.timeout_ns,
                                          FP8Q_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, got)) return false;
-      tphase ^= 1u << buf;
+      tphase ^= 1u << buf_acc;
       tc_fence_after();
       constexpr int kChunks = kEpiCols / 16;
       const uint32_t taddr = tmem_base + lane_addr +
-                             static_cast<uint32_t>(buf * BN + col_half * kEpiCols);
+                             static_cast<uint32_t>(buf_acc * BN + col_half * kEpiCols);
       const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
-      const int m = tl.m0 + row_in_tile;
       const int ncol0 = tl.n0 + col_half * kEpiCols;
-      const bool row_ok = m < tl.row_end && ncol0 < p.N;
-      const bool full = ncol0 + kEpiCols <= p.N;
+      const int wrow0 = tl.m0 + row_in_tile - lane;
+      const bool warp_ok = wrow0 < tl.row_end && ncol0 < p.N;  // warp-uniform
+      const uint32_t buf = smem_u32(sC) + static_cast<uint32_t>(ew) * 2048u;
       if (kOutF32) {
         // FP32 out: two halves of kEpiCols / 2 columns, the first stored while
         // the second is read, which halves the registers the drain holds; the
-        // accumulator is released after the last TMEM read
+        // accumulator is released after the last TMEM read.  Stores go 64
+        // bytes (16 columns) of each row at a time through the warp's buffer.
         constexpr int kHalf = kChunks / 2;
-        float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t v[kHalf][16];
@@ -451,31 +458,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hf == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf) * 8u);
+            if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf_acc) * 8u);
           }
-          if (!row_ok) continue;
+          if (!warp_ok) continue;
 #pragma unroll
-          for (int jj = 0; jj < kHalf * 16; jj += 4) {
-            const int j = hf * kHalf * 16 + jj;
-            float x[4];
+          for (int i = 0; i < kHalf; ++i) {
+            const int col = ncol0 + (hf * kHalf + i) * 16;
+            if (col >= p.N) break;
+            uint4 u[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(v[(jj + e) / 16][(jj + e) % 16]);
-            if (full || ncol0 + j + 4 <= p.N) {
-              if (kAccum) {
-                const float4 old = *reinterpret_cast<const float4 *>(crow + j);
-                x[0] = __fadd_rn(old.x, x[0]);
-                x[1] = __fadd_rn(old.y, x[1]);
-                x[2] = __fadd_rn(old.z, x[2]);
-                x[3] = __fadd_rn(old.w, x[3]);
-              }
-              *reinterpret_cast<float4 *>(crow + j) = make_float4(x[0], x[1], x[2], x[3]);
-            } else {
-              for (int e = 0; e < 4; ++e)
-                if (ncol0 + j + e < p.N) crow[j + e] = kAccum ? __fadd_rn(crow[j + e], x[e]) : x[e];
-            }
+            for (int q = 0; q < 4; ++q)
+              u[q] = make_uint4(v[i][4 * q], v[i][4 * q + 1], v[i][4 * q + 2], v[i][4 * q + 3]);
+            warp_store_block64<4, kAccum>(buf, u, p.c, p.ldc, wrow0, tl.row_end, col, p.N, lane);
           }
         }
-      } else {  // BF16 out
+      } else {  // BF16 out: 64 bytes (32 columns) of each row at a time
         uint32_t v[kChunks][16];
 #pragma unroll
         for (int i = 0; i < kChunks; ++i) tmem_ld_32x32b_x16(taddr + i * 16, v[i]);
@@ -484,28 +481,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 1; i < kChunks; ++i) reg_tie(v[i]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf) * 8u);
-        if (row_ok) {
-          __nv_bfloat16 *crow =
-              static_cast<__nv_bfloat16 *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
+        if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf_acc) * 8u);
+        if (warp_ok) {
 #pragma unroll
-          for (int j = 0; j < kEpiCols; j += 8) {
-            uint32_t w[4];
+          for (int i = 0; i < kChunks; i += 2) {
+            const int col = ncol0 + i * 16;
+            if (col >= p.N) break;
+            uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c0 = j + 2 * e;
+            for (int e = 0; e < 16; ++e) {
+              const int c0 = i * 16 + 2 * e;
               __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[c0 / 16][c0 % 16]),
                                                        __uint_as_float(v[c0 / 16][c0 % 16 + 1]));
               w[e] = *reinterpret_cast<uint32_t *>(&h);
             }
-            if (full || ncol0 + j + 8 <= p.N) {
-              *reinterpret_cast<uint4 *>(crow + j) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
-              for (int e = 0; e < 8; ++e)
-                if (ncol0 + j + e < p.N)
-                  reinterpret_cast<uint16_t *>(crow)[j + e] =
-                      static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
-            }
+            uint4 u[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              u[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            warp_store_block64<2, false>(buf, u, p.c, p.ldc, wrow0, tl.row_end, col, p.N, lane);
           }
         }
       }
