@@ -422,18 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // segments (the thread-per-row layout would touch 32 lines).
       // Grouped tiles: 32-byte column chunks staged in two 1 KB buffers
       // (32-byte swizzle) leave as TMA tensor stores, two per round, which
-      // drain while the next tile is folded.  Thread-level stores remain for
-      // C += (read-modify-write), for per-column B scales, for a grouped warp
-      // whose rows cross the expert's end (the tensor map only clips at M),
-      // and for a last tensor-store chunk that ends inside a 16-byte unit
-      // (tensor stores clip the inner dimension at 16-byte granularity).
+      // drain while the next tile is folded.  C += is a coalesced
+      // read-modify-write (dense only).  Thread-level stores remain for a
+      // grouped warp whose rows cross the expert's end (the tensor map only
+      // clips at M) and for a last tensor-store chunk that ends inside a
+      // 16-byte unit (tensor stores clip the inner dimension at 16-byte
+      // granularity).
       constexpr int kEsz = kOutF32 ? 4 : 2;
       constexpr int kChunkCols = 32 / kEsz;
       const int wrow0 = tl.a_row + row_in_tile - lane;
-      // (per-column scales: the heavier fold leaves no registers for the
-      // staging paths without spills, and those cost more than they save)
-      constexpr bool kStaged = !kAccum && kBScale != FP8Q_BSCALE_ROW;
-      const bool staged = kStaged && (!kGrouped || wrow0 + 32 <= tl.row_end);
+      const bool staged = !kGrouped || wrow0 + 32 <= tl.row_end;
       const bool n_exact = (p.N * kEsz) % 16 == 0;
       auto store_direct = [&](int j0, int j1) {  // columns [j0, j1) of the thread's segment
         if (!(m < tl.row_end)) return;
@@ -485,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (ncol0 < p.N && wrow0 < tl.row_end) {
         int d0 = 0, d1 = staged ? 0 : kEpiCols;  // columns left to thread-level stores
-        if (kStaged && !kGrouped) {
+        if (!kGrouped) {
           // coalesced: 64 bytes of each row at a time through the warp's 2 KB
           constexpr int kRowCols = 64 / kEsz;
           const uint32_t buf = smem_u32(sC) + ew * (2 * kStageCBuf);
@@ -512,11 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int q = 0; q < 4; ++q)
                 u[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
-            warp_store_block64<kEsz, false>(buf, u, p.c, p.ldc, wrow0, tl.row_end, ncol0 + j,
+            warp_store_block64<kEsz, kAccum>(buf, u, p.c, p.ldc, wrow0, tl.row_end, ncol0 + j,
                                             p.N, lane);
           }
         }
-        if (kStaged && kGrouped && wrow0 + 32 <= tl.row_end) {
+        if (kGrouped && staged) {
           // leading chunks that go out as tensor stores; a ragged last chunk
           // (ending inside a 16-byte unit) is left to thread-level stores
           const int cols = min(kEpiCols, p.N - ncol0);

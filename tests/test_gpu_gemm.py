@@ -247,3 +247,33 @@ def test_gemm_accumulate_keeps_existing_values_for_k_zero():
     B.fp8q_gemm_accumulate(a, sa, b, sb, c)
     torch.cuda.synchronize()
     assert torch.all(c == 1.5)
+
+
+@pytest.mark.parametrize("kind", ["block", "block_t"])
+def test_gemm_accumulate_block_scales(oracle, kind):
+    # C (FP32, random start values) += the block-scaled product, Fprop and
+    # Dgrad scale layouts; ragged M and N
+    M, N, K = 300, 392 if kind == "block" else 384, 640
+    x = synth.activation(M, K, seed=81, name="accb.X")
+    qa, sa = B.fp8q_quant_act(bf16_to_torch(x))
+    qa_r, sa_r = oracle.quant_act(x)
+    if kind == "block":
+        w = synth.weight(N, K, seed=82, name="accb.W")
+        qb, sb = B.fp8q_quant_weight(bf16_to_torch(w))
+        qb_r, sb_r = oracle.quant_weight(w)
+        bk, okind = B.FP8Q_BSCALE_BLOCK, oracle.BSCALE_BLOCK
+    else:
+        w = synth.weight(K, N, seed=83, name="accb.Wt")
+        _, sb, qb = B.fp8q_quant_weight(bf16_to_torch(w), with_transpose=True)
+        qw_r, sb_r = oracle.quant_weight(w)
+        qb_r = np.ascontiguousarray(qw_r.T)
+        bk, okind = B.FP8Q_BSCALE_BLOCK_T, oracle.BSCALE_BLOCK_T
+    c0 = np.random.default_rng(84).standard_normal((M, N)).astype(np.float32)
+    c = torch.from_numpy(c0).cuda()
+    B.fp8q_gemm_accumulate(qa, sa, qb, sb, c, bscale_kind=bk)
+    torch.cuda.synchronize()
+    prod, ad = oracle.gemm_rows(qa_r, sa_r, qb_r, sb_r, okind)
+    ref = c0.astype(np.float64) + prod
+    # the product's bound, plus the one FP32 rounding of the addition
+    tol = 2e-4 * ad + np.abs(ref) * 2.0 ** -24 + 1e-30
+    assert_within_tolerance(f64(c), ref, tol, f"accumulate {kind}")

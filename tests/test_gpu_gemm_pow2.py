@@ -245,3 +245,19 @@ def test_pow2_grouped_moe_workload_sampled(oracle):
     rows = np.array(sorted(rows), np.int64)
     ref, ad = oracle.grouped_gemm_rows(qa_r, sa_r, qb_r, sb_r, offs, rows)
     _check(c[torch.from_numpy(rows).cuda()], ref, ad, True, "pow2 moe up-proj")
+
+
+def test_pow2_accumulate_block_scales(oracle):
+    # C (FP32, random start values) += the power-of-two block-scaled product
+    M, N, K = 300, 392, 640
+    x = synth.activation(M, K, seed=91, name="p2accb.X")
+    w = synth.weight(N, K, seed=92, name="p2accb.W")
+    (qa, sa, qb, sb), (qa_r, sa_r, qb_r, sb_r) = _fprop_operands(oracle, x, w)
+    c0 = np.random.default_rng(93).standard_normal((M, N)).astype(np.float32)
+    c = torch.from_numpy(c0).cuda()
+    B.fp8q_gemm_pow2_accumulate(qa, sa, qb, sb, c)
+    torch.cuda.synchronize()
+    prod, ad = oracle.gemm_rows(qa_r, sa_r, qb_r, sb_r, oracle.BSCALE_BLOCK)
+    ref = c0.astype(np.float64) + prod
+    tol = 2e-4 * ad + np.abs(ref) * 2.0 ** -24 + 1e-30
+    assert_within_tolerance(f64(c), ref, tol, "pow2 accumulate block")
