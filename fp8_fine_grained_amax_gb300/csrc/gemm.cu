@@ -84,11 +84,12 @@ constexpr bool kDensePair = true;    // tile shape of the dense GEMMs
 //              128 rows of A and 128 rows (half the columns) of B, and one
 //              tcgen05.mma.cta_group::2 (M = 256) in the leading CTA reads both
 //              CTAs' shared memory and writes both CTAs' tensor memory.  Per SM
-//              that is 32 KB of operands per K-group instead of 48 KB, so six
-//              stages fit and each stage is refilled with a third less traffic.
+//              that is 32 KB of operands per K-group instead of 48 KB, refilled
+//              with a third less traffic; four stages (measured as fast as
+//              six) leave 64 KB for the output staging.
 template <bool kPair>
 struct Cfg {
-  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kStages = kPair ? 4 : 2;
   static constexpr uint32_t kABytes = BM * BK;                    // per CTA
   static constexpr uint32_t kBBytes = (kPair ? BN / 2 : BN) * BK;  // per CTA
   static constexpr int kTileM = kPair ? 2 * BM : BM;              // C rows per tile
@@ -147,16 +148,18 @@ struct alignas(8) SmemCtl {
   alignas(16) float sb_warp[kEpiWarps][2][kEpiCols];
 };
 
-// Output staging: each epilogue warp owns two 1 KB buffers of 32 rows x 32
-// bytes (16 BF16 or 8 FP32 columns), written in the 32-byte swizzle and
-// drained to global memory by TMA tensor stores.
-constexpr uint32_t kStageCBuf = 32 * 32;
-constexpr uint32_t kStageCBytes = kEpiWarps * 2 * kStageCBuf;
+// Output staging: 8 KB per epilogue warp: its 32 rows x 128 BF16 columns as
+// two 32-row x 128-byte boxes for TMA tensor stores (grouped GEMM), or, in
+// its first 2 KB, the 32 x 64-byte blocks of the coalesced stores.
+constexpr uint32_t kStageWarpBytes = 8192;
+constexpr uint32_t kStageCBytes = kEpiWarps * kStageWarpBytes;
 
 __host__ __device__ constexpr size_t smem_bytes(bool grouped, bool pair) {
   return 1024 /* alignment slack */ + (pair ? Cfg<true>::kTileBytes : Cfg<false>::kTileBytes) +
          kStageCBytes + sizeof(SmemCtl) + (grouped ? 2 * (kMaxGroups + 1) * sizeof(int) : 0);
 }
+static_assert(smem_bytes(true, true) <= 227 * 1024 && smem_bytes(true, false) <= 227 * 1024,
+              "shared memory per CTA");
 
 struct Tile {
   int a_row;    // first row of A (and of C) covered by the tile (first CTA of a pair)
@@ -416,77 +419,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---- store this warp's 32 rows x kEpiCols columns
-      // Dense tiles: 64 bytes of each row at a time go through a 2 KB
-      // shared-memory buffer (64-byte swizzle) and leave as 16-byte stores,
-      // four lanes per row, so one instruction writes eight whole 64-byte row
-      // segments (the thread-per-row layout would touch 32 lines).
-      // Grouped tiles: 32-byte column chunks staged in two 1 KB buffers
-      // (32-byte swizzle) leave as TMA tensor stores, two per round, which
-      // drain while the next tile is folded.  C += is a coalesced
-      // read-modify-write (dense only).  Thread-level stores remain for a
-      // grouped warp whose rows cross the expert's end (the tensor map only
-      // clips at M) and for a last tensor-store chunk that ends inside a
-      // 16-byte unit (tensor stores clip the inner dimension at 16-byte
-      // granularity).
+      // Coalesced 64-byte blocks through the first 2 KB of the warp's 8 KB of
+      // shared memory (each 16-byte store instruction writes eight whole
+      // 64-byte row segments).  Grouped BF16 instead puts the whole block
+      // into the 8 KB (two 32-row x 128-byte boxes, 128-byte swizzle) and
+      // writes it with two TMA tensor stores, which drain while the next tile
+      // is folded, unless the warp's rows cross the expert's end (the tensor
+      // map only clips at M) or its row segment ends inside a 16-byte unit
+      // past N (tensor stores clip the inner dimension at 16-byte
+      // granularity).  (In the dense BF16 kernels the tensor-store path cost
+      // registers, and spills, that the fold needs.)
       constexpr int kEsz = kOutF32 ? 4 : 2;
-      constexpr int kChunkCols = 32 / kEsz;
       const int wrow0 = tl.a_row + row_in_tile - lane;
-      const bool staged = !kGrouped || wrow0 + 32 <= tl.row_end;
-      const bool n_exact = (p.N * kEsz) % 16 == 0;
-      auto store_direct = [&](int j0, int j1) {  // columns [j0, j1) of the thread's segment
-        if (!(m < tl.row_end)) return;
-        const bool full = ncol0 + kEpiCols <= p.N;
-        if (kOutF32) {
-          float *crow = static_cast<float *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
+      if (ncol0 < p.N && wrow0 < tl.row_end) {
+        const uint32_t stage = smem_u32(sC) + static_cast<uint32_t>(ew) * kStageWarpBytes;
+        const bool rows_all = !kGrouped || wrow0 + 32 <= tl.row_end;
+        const bool cols_ok = (p.N * kEsz) % 16 == 0 || ncol0 + kEpiCols <= p.N;
+        // the previous tile's tensor stores must have read the buffer
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        if (kGrouped && !kOutF32 && rows_all && cols_ok) {
+          static_assert(kEpiCols == 128, "two 64-column boxes per warp");
 #pragma unroll
-          for (int j = 0; j < kEpiCols; j += 4) {
-            if (j < j0 || j >= j1 || (!full && ncol0 + j >= p.N)) continue;
-            const float2 lo = unpack_f32x2(acc[j / 2]), hi = unpack_f32x2(acc[j / 2 + 1]);
-            float v[4] = {lo.x, lo.y, hi.x, hi.y};
-            if (full || ncol0 + j + 4 <= p.N) {
-              if (kAccum) {  // C += result: one FP32 addition per element
-                const float4 old = *reinterpret_cast<const float4 *>(crow + j);
-                v[0] = __fadd_rn(old.x, v[0]);
-                v[1] = __fadd_rn(old.y, v[1]);
-                v[2] = __fadd_rn(old.z, v[2]);
-                v[3] = __fadd_rn(old.w, v[3]);
-              }
-              *reinterpret_cast<float4 *>(crow + j) = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-              for (int e = 0; e < 4; ++e)
-                if (ncol0 + j + e < p.N) crow[j + e] = kAccum ? __fadd_rn(crow[j + e], v[e]) : v[e];
-            }
-          }
-        } else {
-          __nv_bfloat16 *crow =
-              static_cast<__nv_bfloat16 *>(p.c) + static_cast<int64_t>(m) * p.ldc + ncol0;
-#pragma unroll
-          for (int j = 0; j < kEpiCols; j += 8) {
-            if (j < j0 || j >= j1 || (!full && ncol0 + j >= p.N)) continue;
+          for (int q = 0; q < 16; ++q) {  // 16-byte unit q: columns 8q .. 8q+7
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 v = unpack_f32x2(acc[j / 2 + e]);
+              const float2 v = unpack_f32x2(acc[4 * q + e]);
               __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
               w[e] = *reinterpret_cast<uint32_t *>(&h);
             }
-            if (full || ncol0 + j + 8 <= p.N) {
-              *reinterpret_cast<uint4 *>(crow + j) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
-              for (int e = 0; e < 8; ++e)
-                if (ncol0 + j + e < p.N)
-                  reinterpret_cast<uint16_t *>(crow)[j + e] =
-                      static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
-            }
+            st_shared_v4(stage + (q >> 3) * 4096 + lane * 128 + 16 * ((q & 7) ^ (lane & 7)),
+                         make_uint4(w[0], w[1], w[2], w[3]));
           }
-        }
-      };
-      if (ncol0 < p.N && wrow0 < tl.row_end) {
-        int d0 = 0, d1 = staged ? 0 : kEpiCols;  // columns left to thread-level stores
-        if (!kGrouped) {
-          // coalesced: 64 bytes of each row at a time through the warp's 2 KB
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, stage, ncol0, wrow0);
+            if (ncol0 + 64 < p.N) tma_store_2d(&tmC, stage + 4096, ncol0 + 64, wrow0);
+            bulk_commit_group();
+          }
+        } else {
           constexpr int kRowCols = 64 / kEsz;
-          const uint32_t buf = smem_u32(sC) + ew * (2 * kStageCBuf);
 #pragma unroll
           for (int j = 0; j < kEpiCols; j += kRowCols) {
             if (ncol0 + j >= p.N) break;
@@ -510,70 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int q = 0; q < 4; ++q)
                 u[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
-            warp_store_block64<kEsz, kAccum>(buf, u, p.c, p.ldc, wrow0, tl.row_end, ncol0 + j,
-                                            p.N, lane);
+            warp_store_block64<kEsz, kAccum>(stage, u, p.c, p.ldc, wrow0, tl.row_end, ncol0 + j,
+                                             p.N, lane);
           }
         }
-        if (kGrouped && staged) {
-          // leading chunks that go out as tensor stores; a ragged last chunk
-          // (ending inside a 16-byte unit) is left to thread-level stores
-          const int cols = min(kEpiCols, p.N - ncol0);
-          const int n_chunks = n_exact ? (cols + kChunkCols - 1) / kChunkCols : cols / kChunkCols;
-          if (n_chunks * kChunkCols < cols) {
-            d0 = n_chunks * kChunkCols;
-            d1 = d0 + kChunkCols;
-          }
-          auto pack = [&](int j, uint4 (&u)[2]) {
-            if (kOutF32) {
-              u[0] = make_uint4(static_cast<uint32_t>(acc[j / 2]),
-                                static_cast<uint32_t>(acc[j / 2] >> 32),
-                                static_cast<uint32_t>(acc[j / 2 + 1]),
-                                static_cast<uint32_t>(acc[j / 2 + 1] >> 32));
-              u[1] = make_uint4(static_cast<uint32_t>(acc[j / 2 + 2]),
-                                static_cast<uint32_t>(acc[j / 2 + 2] >> 32),
-                                static_cast<uint32_t>(acc[j / 2 + 3]),
-                                static_cast<uint32_t>(acc[j / 2 + 3] >> 32));
-            } else {
-              uint32_t w[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float2 v = unpack_f32x2(acc[j / 2 + e]);
-                __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
-                w[e] = *reinterpret_cast<uint32_t *>(&h);
-              }
-              u[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              u[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-          };
-          const uint32_t buf0 = smem_u32(sC) + 2 * ew * kStageCBuf;
-          const uint32_t sw = (lane >> 2) & 1;
-#pragma unroll
-          for (int j = 0; j < kEpiCols; j += 2 * kChunkCols) {
-            const int c = j / kChunkCols;
-            if (c >= n_chunks) break;
-            const bool two = c + 1 < n_chunks;
-            uint4 u0[2], u1[2];
-            pack(j, u0);
-            if (two) pack(j + kChunkCols, u1);
-            // both buffers' previous stores must have read them
-            if (lane == 0) bulk_wait_group_read<0>();
-            __syncwarp();
-            st_shared_v4(buf0 + lane * 32 + 16 * sw, u0[0]);
-            st_shared_v4(buf0 + lane * 32 + 16 * (sw ^ 1), u0[1]);
-            if (two) {
-              st_shared_v4(buf0 + kStageCBuf + lane * 32 + 16 * sw, u1[0]);
-              st_shared_v4(buf0 + kStageCBuf + lane * 32 + 16 * (sw ^ 1), u1[1]);
-            }
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmC, buf0, ncol0 + j, wrow0);
-              if (two) tma_store_2d(&tmC, buf0 + kStageCBuf, ncol0 + j + kChunkCols, wrow0);
-              bulk_commit_group();
-            }
-          }
-        }
-        if (d1 > d0) store_direct(d0, d1);
       }
     }
     // every tensor store of this warp has written global memory
@@ -726,13 +640,13 @@ bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// C [rows][cols] (BF16 or FP32) with row pitch ld elements, box 32 rows x 32
-// bytes in the 32-byte swizzle: the epilogue's staged output chunks.
+// C [rows][cols] (BF16 or FP32) with row pitch ld elements, box 32 rows x 128
+// bytes in the 128-byte swizzle: the epilogue's staged output boxes.
 bool make_tmap_c(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, uint64_t ld,
                  bool f32) {
   return make_tmap_2d(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      base, rows, cols, ld * (f32 ? 4 : 2), f32 ? 8 : 16, 32,
-                      CU_TENSOR_MAP_SWIZZLE_32B);
+                      base, rows, cols, ld * (f32 ? 4 : 2), f32 ? 32 : 64, 32,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Launch one instantiation.  `work_tiles` is the number of output tiles (an
