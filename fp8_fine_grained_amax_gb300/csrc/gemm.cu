@@ -207,7 +207,11 @@ __device__ __forceinline__ Tile tile_of(int t, const GemmArgs &p, const int *s_l
   return r;
 }
 
-template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false>
+// kTmaOut (dense BF16, N a multiple of 8): C leaves only as whole-block TMA
+// tensor stores; without the coalesced-store path in the same kernel the fold
+// keeps its registers.
+template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false,
+          bool kTmaOut = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8q_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
@@ -419,16 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---- store this warp's 32 rows x kEpiCols columns
-      // Coalesced 64-byte blocks through the first 2 KB of the warp's 8 KB of
-      // shared memory (each 16-byte store instruction writes eight whole
-      // 64-byte row segments).  Grouped BF16 instead puts the whole block
-      // into the 8 KB (two 32-row x 128-byte boxes, 128-byte swizzle) and
-      // writes it with two TMA tensor stores, which drain while the next tile
-      // is folded, unless the warp's rows cross the expert's end (the tensor
-      // map only clips at M) or its row segment ends inside a 16-byte unit
-      // past N (tensor stores clip the inner dimension at 16-byte
-      // granularity).  (In the dense BF16 kernels the tensor-store path cost
-      // registers, and spills, that the fold needs.)
+      // BF16 (dense with N a multiple of 8, and grouped): the whole block goes
+      // into the warp's 8 KB of shared memory (two 32-row x 128-byte boxes,
+      // 128-byte swizzle) and leaves as two TMA tensor stores, which drain
+      // while the next tile is folded.  Otherwise (FP32, C +=, a grouped warp
+      // whose rows cross the expert's end -- the tensor map only clips at M
+      // -- or a row segment ending inside a 16-byte unit past N -- tensor
+      // stores clip the inner dimension at 16-byte granularity): coalesced
+      // 64-byte blocks through the first 2 KB (each 16-byte store instruction
+      // writes eight whole 64-byte row segments).
       constexpr int kEsz = kOutF32 ? 4 : 2;
       const int wrow0 = tl.a_row + row_in_tile - lane;
       if (ncol0 < p.N && wrow0 < tl.row_end) {
@@ -438,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous tile's tensor stores must have read the buffer
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
-        if (kGrouped && !kOutF32 && rows_all && cols_ok) {
+        static_assert(!kTmaOut || (!kOutF32 && !kAccum && !kGrouped), "dense BF16 only");
+        if (kTmaOut || (kGrouped && !kOutF32 && rows_all && cols_ok)) {
           static_assert(kEpiCols == 128, "two 64-column boxes per warp");
 #pragma unroll
           for (int q = 0; q < 16; ++q) {  // 16-byte unit q: columns 8q .. 8q+7
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ncol0 + 64 < p.N) tma_store_2d(&tmC, stage + 4096, ncol0 + 64, wrow0);
             bulk_commit_group();
           }
-        } else {
+        } else if (!kTmaOut) {
           constexpr int kRowCols = 64 / kEsz;
 #pragma unroll
           for (int j = 0; j < kEpiCols; j += kRowCols) {
@@ -652,10 +656,11 @@ bool make_tmap_c(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, uint6
 // Launch one instantiation.  `work_tiles` is the number of output tiles (an
 // upper bound for the grouped GEMM); the grid is persistent: one CTA (or one
 // CTA pair) per SM that can hold one, never more than there are tiles.
-template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false>
+template <int kBScale, bool kOutF32, bool kGrouped, bool kPair, bool kAccum = false,
+          bool kTmaOut = false>
 fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                    const GemmArgs &args, int64_t work_tiles, cudaStream_t s) {
-  auto kern = fp8q_gemm_kernel<kBScale, kOutF32, kGrouped, kPair, kAccum>;
+  auto kern = fp8q_gemm_kernel<kBScale, kOutF32, kGrouped, kPair, kAccum, kTmaOut>;
   const size_t smem = smem_bytes(kGrouped, kPair);
   static int max_units[kMaxDevices] = {};  // co-resident CTAs (or CTA pairs) per device
   static std::mutex mu;
@@ -722,16 +727,25 @@ fp8q_status dispatch(int bkind, bool f32, const CUtensorMap &ta, const CUtensorM
     return f32 ? launch<FP8Q_BSCALE_BLOCK, true, true, kGroupedPair>(ta, tb, tc, a, tiles, s)
                : launch<FP8Q_BSCALE_BLOCK, false, true, kGroupedPair>(ta, tb, tc, a, tiles, s);
   }
+  // BF16 rows that end on a 16-byte unit take the tensor-store-only kernels
+  const bool tma = !f32 && a.N % 8 == 0;
   switch (bkind) {
     case FP8Q_BSCALE_BLOCK:
-      return f32 ? launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
-                 : launch<FP8Q_BSCALE_BLOCK, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
+      return f32   ? launch<FP8Q_BSCALE_BLOCK, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
+             : tma ? launch<FP8Q_BSCALE_BLOCK, false, false, kDensePair, false, true>(
+                         ta, tb, tc, a, tiles, s)
+                   : launch<FP8Q_BSCALE_BLOCK, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
     case FP8Q_BSCALE_BLOCK_T:
-      return f32 ? launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
-                 : launch<FP8Q_BSCALE_BLOCK_T, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
+      return f32   ? launch<FP8Q_BSCALE_BLOCK_T, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
+             : tma ? launch<FP8Q_BSCALE_BLOCK_T, false, false, kDensePair, false, true>(
+                         ta, tb, tc, a, tiles, s)
+                   : launch<FP8Q_BSCALE_BLOCK_T, false, false, kDensePair>(ta, tb, tc, a, tiles,
+                                                                           s);
     default:
-      return f32 ? launch<FP8Q_BSCALE_ROW, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
-                 : launch<FP8Q_BSCALE_ROW, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
+      return f32   ? launch<FP8Q_BSCALE_ROW, true, false, kDensePair>(ta, tb, tc, a, tiles, s)
+             : tma ? launch<FP8Q_BSCALE_ROW, false, false, kDensePair, false, true>(
+                         ta, tb, tc, a, tiles, s)
+                   : launch<FP8Q_BSCALE_ROW, false, false, kDensePair>(ta, tb, tc, a, tiles, s);
   }
 }
 

@@ -183,3 +183,28 @@ def test_strided_operands_and_output(oracle, mode, kind):
     ref, ad = oracle.gemm_rows(qa_r, sa_r, qb_r, sb_r, okind)
     _check(c_v, ref, ad, out == B.FP8Q_OUT_BF16, f"{mode} strided {kind}")
     assert torch.all(c_buf[:, N:] == -5.0), "padding of C was written"
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("N", [300, 13])
+def test_bf16_rows_ending_inside_a_16_byte_unit(oracle, mode, N):
+    # BF16 rows of N % 8 != 0 columns end inside a 16-byte unit: the kernels
+    # must not write the padding of C (pitch rounded up to 16 bytes)
+    p2 = mode == "pow2"
+    sm = _scale_mode(mode)
+    M, K = 200, 384
+    x = synth.activation(M, K, seed=31, name="ragged.X")
+    w = synth.weight(N, K, seed=32, name="ragged.W")
+    qa, sa = B.fp8q_quant_act(bf16_to_torch(x), scale_mode=sm)
+    qb, sb = B.fp8q_quant_weight(bf16_to_torch(w), scale_mode=sm)
+    qa_r, sa_r = oracle.quant_act(x, p2)
+    qb_r, sb_r = oracle.quant_weight(w, p2)
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(qb), qb_r, "B codes")
+    ldc = (N + 7) // 8 * 8
+    c_buf = torch.full((M, ldc), -5.0, dtype=torch.bfloat16, device="cuda")
+    _gemm(mode)(qa, sa, qb, sb, c=c_buf[:, :N])
+    torch.cuda.synchronize()
+    ref, ad = oracle.gemm_rows(qa_r, sa_r, qb_r, sb_r, oracle.BSCALE_BLOCK)
+    _check(c_buf[:, :N], ref, ad, True, f"{mode} ragged N={N}")
+    assert torch.all(c_buf[:, N:] == -5.0), "padding of C was written"
