@@ -208,3 +208,63 @@ def test_bf16_rows_ending_inside_a_16_byte_unit(oracle, mode, N):
     ref, ad = oracle.gemm_rows(qa_r, sa_r, qb_r, sb_r, oracle.BSCALE_BLOCK)
     _check(c_buf[:, :N], ref, ad, True, f"{mode} ragged N={N}")
     assert torch.all(c_buf[:, N:] == -5.0), "padding of C was written"
+
+
+def _effective_offsets(offs, M):
+    """Expert row ranges as the grouped GEMM's interface defines them for
+    offsets that break the ordering: clamp into [0, M]; an expert starts no
+    earlier than the previous one ended; a decreasing step is an empty expert."""
+    c = np.clip(offs.astype(np.int64), 0, M)
+    eff = np.zeros_like(c)
+    prev_hi = 0
+    for g in range(offs.size - 1):
+        lo = max(c[g], prev_hi)
+        hi = max(lo, c[g + 1])
+        eff[g] = lo
+        prev_hi = hi
+    eff[-1] = prev_hi
+    return eff.astype(np.int32)
+
+
+def _grouped(mode):
+    return B.fp8q_grouped_gemm_pow2 if mode == "pow2" else B.fp8q_grouped_gemm
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("case", ["max_experts", "unordered_offsets"])
+def test_grouped_gemm_offset_edge_cases(oracle, mode, case):
+    p2 = mode == "pow2"
+    sm = _scale_mode(mode)
+    N, K = 136, 256
+    if case == "max_experts":
+        # 1024 experts (the most one call takes) over 3000 tokens, a third empty
+        G, M = 1024, 3000
+        rng = np.random.default_rng(41)
+        counts = rng.integers(0, 6, G) * (rng.random(G) > 0.33)
+        counts[-1] += M - counts.sum() if counts.sum() < M else 0
+        offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+        offs = np.minimum(offs, M).astype(np.int32)
+    else:
+        # offsets past M, a decreasing step and a negative start: clamped
+        G, M = 6, 700
+        offs = np.array([-5, 120, 90, 300, 301, 900, 650], np.int32)
+    eff = _effective_offsets(offs, M)
+    x = synth.activation(M, K, seed=42, name="goff.X")
+    wq = np.empty((G, N, K), np.uint8)
+    ws = np.empty((G, (N + 127) // 128, K // 128), np.float32)
+    for g in range(G):
+        wq[g], ws[g] = oracle.quant_weight(synth.weight(N, K, seed=1000 + g, name="goff.W"), p2)
+    qa, sa = B.fp8q_quant_act(bf16_to_torch(x), scale_mode=sm)
+    qa_r, sa_r = oracle.quant_act(x, p2)
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(qa), qa_r, "A codes")
+    c = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    _grouped(mode)(qa, sa, torch.from_numpy(wq).cuda(), torch.from_numpy(ws).cuda(),
+                   torch.from_numpy(offs).cuda(), c=c)
+    torch.cuda.synchronize()
+    inside = np.arange(int(eff[0]), int(eff[-1]))
+    ref, ad = oracle.grouped_gemm_rows(qa_r, sa_r, wq, ws, eff, inside)
+    _check(c[torch.from_numpy(inside).cuda()], ref, ad, True, f"{mode} grouped {case}")
+    outside = np.setdiff1d(np.arange(M), inside)
+    if outside.size:
+        assert torch.all(c[torch.from_numpy(outside).cuda()] == 3.0), "rows outside the experts written"
