@@ -99,6 +99,26 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t smem_src
       "r"(c0), "r"(c1), "r"(smem_src)
       : "memory");
 }
+// L2 policy that makes the written lines the first to go: for a GEMM's C,
+// which no one reads back while the operands are still being reused.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t smem_src, int32_t c0,
+                                                  int32_t c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(smem_src), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void st_global_v4_hint(void *ptr, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -148,9 +168,10 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // shared-memory buffer `buf`: the units go in under a 64-byte XOR swizzle
 // (unit q of row r at q ^ ((r >> 1) & 3), conflict-free) and come back four
 // lanes per row, so each 16-byte global store writes eight whole 64-byte row
-// segments instead of 32 scattered pieces.  The block starts at (row0, col0);
-// rows >= row_end and columns >= n are left alone.  kEsz: element size (2 or
-// 4); kAccum (FP32 only): C += values, one FP32 addition per element.
+// segments instead of 32 scattered pieces, with an L2 evict-first hint.  The
+// block starts at (row0, col0); rows >= row_end and columns >= n are left
+// alone.  kEsz: element size (2 or 4); kAccum (FP32 only): C += values, one
+// FP32 addition per element.
 template <int kEsz, bool kAccum>
 __device__ __forceinline__ void warp_store_block64(uint32_t buf, const uint4 (&u)[4], void *c,
                                                    int64_t ldc, int row0, int row_end, int col0,
@@ -178,7 +199,7 @@ __device__ __forceinline__ void warp_store_block64(uint32_t buf, const uint4 (&u
         v.z = __float_as_uint(__fadd_rn(old.z, __uint_as_float(v.z)));
         v.w = __float_as_uint(__fadd_rn(old.w, __uint_as_float(v.w)));
       }
-      *reinterpret_cast<uint4 *>(dst) = v;
+      st_global_v4_hint(dst, v, l2_evict_first_policy());
     } else {
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       for (int e = 0; e < kUnitCols && col + e < n; ++e) {

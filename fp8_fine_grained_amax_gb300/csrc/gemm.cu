@@ -459,8 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmC, stage, ncol0, wrow0);
-            if (ncol0 + 64 < p.N) tma_store_2d(&tmC, stage + 4096, ncol0 + 64, wrow0);
+            // C is not read back: evict-first keeps the operands in L2
+            const uint64_t pol = l2_evict_first_policy();
+            tma_store_2d_hint(&tmC, stage, ncol0, wrow0, pol);
+            if (ncol0 + 64 < p.N) tma_store_2d_hint(&tmC, stage + 4096, ncol0 + 64, wrow0, pol);
             bulk_commit_group();
           }
         } else if (!kTmaOut) {
