@@ -13,18 +13,21 @@
 //   warp 0      TMA producer: A and B tiles (128 K-bytes per row, 128-byte
 //               swizzle) into a kStages-deep shared-memory ring, completing
 //               on "full" mbarriers.
-//   warp 1      MMA issuer (one thread): per K-group, 4 x tcgen05.mma
-//               (kind::f8f6f4, M=128, N=256, K=32) into one of two TMEM
-//               partial buffers, then tcgen05.commit to release the ring slot
-//               and to signal the partial.
+//   warp 1      MMA issuer (one thread; in a CTA pair, of the leading CTA):
+//               per K-group, 4 x tcgen05.mma (kind::f8f6f4, K=32, N=256; M=256
+//               across the pair with cta_group::2, each CTA's 128 rows in its
+//               own TMEM) into one of two TMEM partial buffers, then
+//               tcgen05.commit to release the ring slot and to signal the
+//               partial.
 //   warps 2-3   idle (they complete the first warpgroup).
 //   warps 4-11  epilogue: tcgen05.ld the partial (each thread one row, 128
 //               columns, 16 at a time), acc += P * sa(m,kb) * sb(n,kb) in FP32
 //               registers with packed two-lane FMAs (fma.rn.f32x2), release the
 //               TMEM buffer; after the last group, round C to BF16 (nearest
-//               even) or keep FP32 and write it out through a per-warp
-//               shared-memory buffer: coalesced 16-byte stores (dense) or
-//               TMA tensor stores (grouped).  The scales of group kb+1 are
+//               even) or keep FP32 and write it out through 8 KB of shared
+//               memory per warp: BF16 as two 128-byte-swizzled boxes and TMA
+//               tensor stores, otherwise as coalesced 16-byte stores, both
+//               with an L2 evict-first policy.  The scales of group kb+1 are
 //               loaded while group kb is folded.
 //
 // Registers: the kernel is built for 384 threads at 168 registers each (the

@@ -32,7 +32,8 @@
 //               quarter).  At the end of a tile they read its accumulator
 //               (each thread BN/2 columns of its row), release it and store C
 //               through a 2 KB shared-memory buffer per warp, 64 bytes of
-//               each row at a time, as coalesced 16-byte stores.
+//               each row at a time, as coalesced 16-byte stores with an L2
+//               evict-first policy.
 //
 // Shipped shape: BN = 256 with one accumulator (columns 0-255) and 16 scale
 // stages (columns 256-511).  The epilogue writes scale stages up to 6 ahead
