@@ -1,0 +1,77 @@
+"""CPU checks of bench.py's contract: the reference arm's JSON line (the
+oracle timed on the host, tiny workload), argument checks, and the lookup of
+DRAM traffic in the committed ncu summaries."""
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _run(*args, timeout=300):
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+def test_reference_arm_json_line():
+    r = _run("--impl", "reference", "--workload", "tiny_fprop", "--steps", "3", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["vs_baseline"] is None
+    assert d["data"] == "synthetic"
+    assert d["config"]["workload"] == "tiny_fprop"
+    assert d["ms_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_warmup_below_three_is_rejected():
+    r = _run("--impl", "reference", "--workload", "tiny_fprop", "--steps", "3", "--warmup", "2",
+             timeout=120)
+    assert r.returncode != 0
+    assert "warmup" in (r.stderr + r.stdout)
+
+
+def test_unknown_workload_is_rejected():
+    r = _run("--impl", "reference", "--workload", "no_such_workload", "--steps", "3",
+             "--warmup", "3", timeout=120)
+    assert r.returncode != 0
+
+
+@pytest.mark.parametrize("kernel,workload", [
+    ("fp8q_gemm_kernel", "fprop_4096x7168x7168"),
+    ("fp8q_gemm_mx_kernel", "fprop_pow2_4096x7168x7168"),
+    ("no_such_kernel", "fprop_4096x7168x7168"),
+])
+def test_profile_traffic_follows_the_source_hash(kernel, workload):
+    # the traffic of a committed summary is reported only while the kernel's
+    # source still hashes to the value recorded with the counters
+    import bench
+    got = bench.profile_traffic(kernel, workload)
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        assert got is None
+        return
+    text = open(path).read()
+    src = re.search(r"source_file:\s*(\S+)", text).group(1)
+    recorded = re.search(r"source_sha256:\s*([0-9a-f]{64})", text).group(1)
+    cur = hashlib.sha256(open(os.path.join(ROOT, "fp8_fine_grained_amax_gb300", "csrc", src),
+                              "rb").read()).hexdigest()
+    dram = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text).group(1))
+    assert got == (dram if cur == recorded else None)
