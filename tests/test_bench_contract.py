@@ -75,3 +75,33 @@ def test_profile_traffic_follows_the_source_hash(kernel, workload):
                               "rb").read()).hexdigest()
     dram = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text).group(1))
     assert got == (dram if cur == recorded else None)
+
+
+@pytest.mark.gpu
+def test_our_arm_json_line_on_the_gpu():
+    # our arm on the tiny workload: the JSON line carries the keys the
+    # benchmark contract asks for, with the device-resident value, the
+    # end-to-end value through host buffers, the roofline of the dominant
+    # kernel and the launch count of our kernels in the timed region
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    r = _run("--workload", "tiny_fprop", "--steps", "20", "--warmup", "3", "--no-cpu-baseline")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "e2e", "gpu_launches", "clocks"):
+        assert k in d, k
+    assert d["value"] > 0 and d["steps"] == 20 and d["warmup"] == 3
+    assert d["gpu_launches"] == 3 * 20          # quant_act, quant_weight, GEMM per step
+    roof = d["roofline"]
+    assert roof["bound"] == "tensor" and roof["kernel"] == "fp8q_gemm_kernel"
+    assert roof["peak"] > 0 and abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
+    e2e = d["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 2 * (256 * 512 + 256 * 512)   # X and W, BF16
+    assert e2e["d2h_bytes_per_step"] == 2 * 256 * 256                 # C, BF16
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
