@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "fp8q.h"
 
@@ -49,8 +50,21 @@ inline fp8q_status device_info(DeviceInfo &out) {
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-inline fp8q_status launch_status() {
-  return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+// Launch `kern` on stream `s` and report this launch's own outcome: the value
+// cudaLaunchKernelEx returns, not the process-wide last-error state, which may
+// hold an earlier, unrelated error that belongs to the caller (reading it with
+// cudaGetLastError would also clear it).
+template <typename... KArgs, typename... Args>
+inline fp8q_status launch_on(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess
+             ? FP8Q_OK
+             : FP8Q_ERR_CUDA;
 }
 
 // Time limit of every device-side wait (fp8q_set_wait_timeout_ns).

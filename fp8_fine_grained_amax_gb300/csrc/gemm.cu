@@ -705,8 +705,7 @@ fp8q_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorM
   }
   const int64_t units = work_tiles < max_units[dev] ? work_tiles : max_units[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(units * (kPair ? 2 : 1)), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args) != cudaSuccess) return FP8Q_ERR_CUDA;
-  return launch_status();
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args) == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
 // Tile shapes: kDensePair / kGroupedPair select CTA pairs (256 x 256 tiles)
@@ -920,6 +919,6 @@ extern "C" void fp8q_set_wait_timeout_ns(uint64_t ns) {
 extern "C" fp8q_status fp8q_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns);
-  return launch_status();
+  return launch_on(wait_timeout_probe_kernel, dim3(1), dim3(32), 0,
+                   static_cast<cudaStream_t>(stream), timeout_ns);
 }

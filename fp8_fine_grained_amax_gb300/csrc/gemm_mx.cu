@@ -680,8 +680,7 @@ fp8q_status launch_mx(const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs
   }
   const int64_t pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, args) != cudaSuccess) return FP8Q_ERR_CUDA;
-  return launch_status();
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args) == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
 template <bool kAccum>

@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "fp8q.h"
 #include "fp8q_host.cuh"
@@ -649,9 +650,8 @@ fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX,
       attr_set[dev] = true;
     }
   }
-  kern<<<grid, kTileThreads, kActTSmem, s>>>(tmX, tmQ, T, C, sT, ld_sT, q_rows, ldq_rows, s_rows,
-                                             ld_s_rows, timeout_ns);
-  return launch_status();
+  return launch_on(kern, dim3(grid), dim3(kTileThreads), kActTSmem, s, tmX, tmQ, T, C, sT, ld_sT,
+                   q_rows, ldq_rows, s_rows, ld_s_rows, timeout_ns);
 }
 
 constexpr size_t kRequantSmem = 2 * kTileBytesQ + kTileBytesBF16 + 2 * kTileBytesQ + 1024;
@@ -675,9 +675,8 @@ fp8q_status launch_requant(unsigned grid, cudaStream_t s, const CUtensorMap &tmQ
       attr_set[dev] = true;
     }
   }
-  kern<<<grid, kTileThreads, kRequantSmem, s>>>(tmQ, tmQT, T, C, s_rows, ld_s_rows, sT, ld_sT,
-                                                timeout_ns);
-  return launch_status();
+  return launch_on(kern, dim3(grid), dim3(kTileThreads), kRequantSmem, s, tmQ, tmQT, T, C, s_rows,
+                   ld_s_rows, sT, ld_sT, timeout_ns);
 }
 
 constexpr size_t kWeightTSmem = kTileBytesBF16 + kTileBytesQ + 1024;  // transposed path only
@@ -701,8 +700,8 @@ fp8q_status launch_weight(dim3 grid, cudaStream_t s, const uint16_t *w, int64_t 
       attr_set[dev] = true;
     }
   }
-  kern<<<grid, kTileThreads, smem, s>>>(w, N, ldw, q, ldq, tmQT, qT, ldqT, sb, ld_sb);
-  return launch_status();
+  return launch_on(kern, grid, dim3(kTileThreads), smem, s, w, N, ldw, q, ldq, tmQT, qT, ldqT, sb,
+                   ld_sb);
 }
 
 }  // namespace
@@ -727,11 +726,8 @@ extern "C" fp8q_status fp8q_quant_act(const void *x, int64_t M, int64_t K, int64
   auto s = static_cast<cudaStream_t>(stream);
   auto xp = static_cast<const uint16_t *>(x);
   auto qp = static_cast<uint8_t *>(q);
-  if (scale_mode == FP8Q_SCALE_POW2)
-    quant_act_kernel<true><<<grid, 256, 0, s>>>(xp, M, ldx, qp, ldq, sa, ld_sa);
-  else
-    quant_act_kernel<false><<<grid, 256, 0, s>>>(xp, M, ldx, qp, ldq, sa, ld_sa);
-  return launch_status();
+  return launch_on(scale_mode == FP8Q_SCALE_POW2 ? quant_act_kernel<true> : quant_act_kernel<false>,
+                   grid, dim3(256), 0, s, xp, M, ldx, qp, ldq, sa, ld_sa);
 }
 
 extern "C" fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int64_t ldx, void *qT,
@@ -828,9 +824,8 @@ extern "C" fp8q_status fp8q_cast_e4m3(const float *x, int64_t n, void *q, void *
   int64_t blocks = (n4 + 255) / 256;
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
   if (blocks > cap) blocks = cap;
-  cast_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      x, n, static_cast<uint8_t *>(q));
-  return launch_status();
+  return launch_on(cast_e4m3_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                   static_cast<cudaStream_t>(stream), x, n, static_cast<uint8_t *>(q));
 }
 
 extern "C" fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, int64_t ldq,
@@ -867,6 +862,19 @@ extern "C" fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, i
              : launch_requant<false>(grid, s, tmQ, tmQT, T, C, s_rows, ld_s_rows, sT, ld_sT, tmo);
 }
 
+// The two passes of the per-tensor quantiser over the partials array `part`.
+static fp8q_status tensor_passes(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
+                                 int64_t ldq, float *s, uint32_t *part, int64_t P, int scale_mode,
+                                 cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(P));
+  if (fp8q_status e = launch_on(tensor_amax_kernel, grid, dim3(256), 0, st, x, M, K, ldx, part))
+    return e;
+  return launch_on(scale_mode == FP8Q_SCALE_POW2 ? tensor_quant_kernel<true>
+                                                 : tensor_quant_kernel<false>,
+                   grid, dim3(256), 0, st, x, M, K, ldx, q, ldq, s,
+                   static_cast<const uint32_t *>(part), static_cast<int>(P));
+}
+
 static int64_t tensor_partials(int64_t M) { return M > 0 ? (M + kTensorRows - 1) / kTensorRows : 1; }
 
 extern "C" int64_t fp8q_quant_tensor_workspace_bytes(int64_t M, int64_t K) {
@@ -892,14 +900,7 @@ extern "C" fp8q_status fp8q_quant_tensor(const void *x, int64_t M, int64_t K, in
   auto st_ = static_cast<cudaStream_t>(stream);
   auto xp = static_cast<const uint16_t *>(x);
   auto part = static_cast<uint32_t *>(workspace);
-  tensor_amax_kernel<<<static_cast<unsigned>(P), 256, 0, st_>>>(xp, M, K, ldx, part);
-  if (scale_mode == FP8Q_SCALE_POW2)
-    tensor_quant_kernel<true><<<static_cast<unsigned>(P), 256, 0, st_>>>(
-        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
-  else
-    tensor_quant_kernel<false><<<static_cast<unsigned>(P), 256, 0, st_>>>(
-        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
-  return launch_status();
+  return tensor_passes(xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, P, scale_mode, st_);
 }
 
 // ------------------------------------------------------------------ per tensor, no allocation
@@ -916,21 +917,66 @@ extern "C" fp8q_status fp8q_quant_tensor(const void *x, int64_t M, int64_t K, in
 constexpr int64_t kNoAllocPartials = 1024;  // 4 KB per device, held until the process exits
 static __device__ __align__(256) uint32_t g_noalloc_partials[kNoAllocPartials];
 
-// Device address of the array on the current device, looked up once per device.
+// Unique id of the calling thread's current CUDA context, or 0 when no
+// context is current or the driver cannot say (driver entry points looked up
+// through the runtime, as for the tensor-map encoder).
+static uint64_t current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext *);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r) ==
+            cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &r) ==
+            cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the array in the current device's current context.  The
+// address is cached per device together with the id of the context it was
+// looked up in, and looked up again whenever that context is not the current
+// one (after cudaDeviceReset, or after the primary context was released and
+// created anew, the old address belongs to a context that no longer exists).
+// Without a context id the lookup is simply repeated on every call.
 static fp8q_status noalloc_partials(uint32_t **out) {
-  static uint32_t *ptrs[kMaxDevices] = {};
+  struct Slot {
+    uint64_t ctx_id = 0;
+    uint32_t *ptr = nullptr;
+  };
+  static Slot slots[kMaxDevices];
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  if (ptrs[dev] == nullptr) {
+  Slot &slot = slots[dev];
+  const uint64_t now = current_context_id();
+  if (slot.ptr == nullptr || now == 0 || now != slot.ctx_id) {
     uint32_t *ptr = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_partials) != cudaSuccess ||
         ptr == nullptr)
       return FP8Q_ERR_CUDA;
-    ptrs[dev] = ptr;
+    // the lookup makes the device's primary context current if none was
+    slot.ctx_id = current_context_id();
+    slot.ptr = slot.ctx_id != 0 ? ptr : nullptr;
+    *out = ptr;
+    return FP8Q_OK;
   }
-  *out = ptrs[dev];
+  *out = slot.ptr;
   return FP8Q_OK;
 }
 
@@ -952,12 +998,5 @@ extern "C" fp8q_status fp8q_quant_tensor_noalloc(const void *x, int64_t M, int64
   if (fp8q_status st = noalloc_partials(&part)) return st;
   auto st_ = static_cast<cudaStream_t>(stream);
   auto xp = static_cast<const uint16_t *>(x);
-  tensor_amax_kernel<<<static_cast<unsigned>(P), 256, 0, st_>>>(xp, M, K, ldx, part);
-  if (scale_mode == FP8Q_SCALE_POW2)
-    tensor_quant_kernel<true><<<static_cast<unsigned>(P), 256, 0, st_>>>(
-        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
-  else
-    tensor_quant_kernel<false><<<static_cast<unsigned>(P), 256, 0, st_>>>(
-        xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, static_cast<int>(P));
-  return launch_status();
+  return tensor_passes(xp, M, K, ldx, static_cast<uint8_t *>(q), ldq, s, part, P, scale_mode, st_);
 }

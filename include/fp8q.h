@@ -26,9 +26,11 @@
  *     that tensor's type.  E4M3 tensors are raw bytes (1 byte per element),
  *     BF16 tensors raw 16-bit patterns.
  *   - All pointers are DEVICE pointers owned by the caller; the library never
- *     allocates or frees device memory, and keeps no pointer after a call
- *     returns.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is
- *     the legacy default stream).
+ *     allocates or frees device memory, and keeps none of the caller's
+ *     pointers after a call returns (the only device address it keeps is that
+ *     of its own static scratch array, see fp8q_quant_tensor_noalloc).  Calls
+ *     are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).
  *   - E4M3 means the OCP "E4M3FN" encoding (bias 7, largest finite 448, NaN
  *     0x7F/0xFF, no infinity).  Values are rounded to nearest-even and
  *     saturated to +-448.
@@ -169,7 +171,11 @@ fp8q_status fp8q_quant_tensor(const void *x, int64_t M, int64_t K, int64_t ldx,
  *     and launches nothing.  Every other argument, result and error is as for
  *     fp8q_quant_tensor.
  *   - The first call on a device (with that device current) looks up the
- *     array's device address; make that call before any stream capture.
+ *     array's device address; make that call before any stream capture.  The
+ *     address is remembered with the id of the CUDA context it belongs to and
+ *     looked up again when another context is current, e.g. after
+ *     cudaDeviceReset or after the primary context was released and created
+ *     again (the first call after that is again a set-up call).
  *   - Every call on a device uses the same array.  Calls whose kernels
  *     overlap on the GPU (different streams, no ordering between them) race
  *     and may return wrong scales; calls ordered on one stream do not.

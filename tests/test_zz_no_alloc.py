@@ -70,3 +70,26 @@ def test_noalloc_row_limit(lib):
     assert np.all(u8(q[:65536]) == 0)
     assert_bytes_equal(u8(q[:65536]), u8(q_ref), "codes M=65536")
     assert_scales_equal(f32(s), f32(s_ref), "scale M=65536")
+
+
+@pytest.mark.parametrize("mode", [0, 1])   # FP8Q_SCALE_FP32, FP8Q_SCALE_POW2
+@pytest.mark.parametrize("M,K", [(0, 256), (300, 0)])
+def test_noalloc_empty_input_gives_the_zero_tensor_scale(lib, oracle, M, K, mode):
+    # a call on real data first leaves nonzero partials in the shared scratch;
+    # an empty input (no rows, or rows of no columns) must still come out with
+    # the scale of an all-zero tensor, a = 2^-116: its own first pass writes
+    # every partial its second pass reads, so nothing stale is picked up
+    x0 = bf16_to_torch(synth.activation(4096, 1024, seed=703))
+    q0 = torch.empty((4096, 1024), dtype=torch.uint8, device="cuda")
+    s0 = torch.empty((1,), dtype=torch.float32, device="cuda")
+    assert _noalloc(lib, x0, q0, s0, mode) == 0
+    x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    s = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    assert _noalloc(lib, x, q, s, mode) == 0
+    _, s_ws = B.fp8q_quant_tensor(x, scale_mode=mode)
+    _, s_zero = oracle.quant_tensor(np.zeros((1, 128), np.uint16), mode == 1)
+    torch.cuda.synchronize()
+    assert f32(s0)[0] > 0 and f32(s0)[0] != np.float32(s_zero), "first call gave a zero scale"
+    assert_scales_equal(f32(s), f32(s_ws), f"scale M={M} K={K} (workspace form)")
+    assert_scales_equal(f32(s), np.array([s_zero], np.float32), f"scale M={M} K={K} (oracle)")
