@@ -1,28 +1,38 @@
 """Benchmark of the fine-grained FP8 hot path on GB300.
 
 One step = the whole hot path of one workload on seeded synthetic inputs that
-are already resident in HBM.  The default workload is the forward pass of one
+are already resident in HBM.  The headline workload is the forward pass of one
 linear layer, M=4096 tokens, N=7168 outputs, K=7168 inputs:
   quantise the activation X [M][K] (1x128 tiles), quantise the weight W [N][K]
   (128x128 blocks), FP8 GEMM with per-128-K-group scaling, BF16 output.
-Other workloads (--workload):
+Other workloads (--workload, and all of them in the line's "workloads" key):
+  tiny_fprop             256 x 256 x 512 Fprop (the small parity case)
+  fprop_pow2_4096x7168x7168  the headline with power-of-two scales (block-scaled MMA)
   linear_bwd_T8192       Dgrad + Wgrad of a 7168->2048 linear over 8192 tokens,
                          with the 128x1 / fused 1x128 and 128x128 quantisers
+  linear_bwd_pow2_T8192  the same with power-of-two scales
+  linear_bwd_cached_T8192  the backward with X requantised from the FP8 cache
   moe_fprop_16x16384     MoE up- (7168->4096) and down-projection (2048->7168),
                          16 experts, Dirichlet(0.5) top-1 routing, grouped GEMMs
+  moe_fprop_pow2_16x16384  the same with power-of-two scales
   square_<n>             n x n x n Fprop step (quantise both operands + GEMM)
   quant_act_<t>          1x128 quantisation of t x 7168 (GB/s)
   quant_act_pow2_<t>     same with power-of-two scales (GB/s)
   quant_act_T_<t>        128x1 transposed quantisation of t x 7168 (GB/s)
-  quant_weight_<g>x4096  128x128 quantisation of g stacked 4096x7168 weights (GB/s)
+  quant_act_T_pow2_<t>   same with power-of-two scales (GB/s)
+  quant_weight_<n>x<k>   128x128 quantisation of one n x k weight (GB/s)
+  quant_weight_<g>x<n>x<k>  the same over g stacked n x k weights (GB/s)
   quant_tensor_<t>       per-tensor quantisation of t x 7168, for comparison (GB/s)
-  linear_bwd_cached_T8192  the backward with X requantised from the FP8 cache
 
 Prints ONE JSON line (rank 0).  `value` is the step's algorithmic work (GEMM
 FLOPs 2MNK over real rows, or quantiser bytes) summed over ranks per second of
-device time.  The per-kernel times, the roofline of the dominant kernel, an
-end-to-end number through host buffers, the clocks seen during the timed
-region and the CPU oracle's throughput on a bounded sample are added.
+device time.  The timed region is the K-step loop, repeated until it has run
+for at least --min-seconds (each repeat between a barrier and a device
+synchronise); the median repeat gives `ms_per_step`.  The per-kernel times, the
+roofline of the dominant kernel, an end-to-end number through host buffers,
+the clocks sampled during the timed region, the error of the result against
+the CPU oracle, the CPU oracle's own throughput, and (one GPU) the same
+per-kernel measurement for every other workload are added.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -34,6 +44,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -49,11 +60,41 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "blockscaled FP8 GEMM TFLOP/s & % FP8 peak; quantize GB/s & % HBM"
+HEADLINE = "fprop_4096x7168x7168"
 L2_BYTES = 126 * 1024 * 1024
 FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor-core rate
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 CSRC = os.path.join(ROOT, "fp8_fine_grained_amax_gb300", "csrc")
+
+# Every configuration's workloads (tiny Fprop; Fprop; linear backward; MoE;
+# quantiser and square-GEMM sweep), each measured after the headline in the
+# same run, with its own timed region.
+CONFIG_WORKLOADS = [
+    ("tiny", "tiny_fprop"),
+    ("fprop", "fprop_pow2_4096x7168x7168"),
+    ("linear_bwd", "linear_bwd_T8192"),
+    ("linear_bwd", "linear_bwd_pow2_T8192"),
+    ("linear_bwd", "linear_bwd_cached_T8192"),
+    ("moe", "moe_fprop_16x16384"),
+    ("moe", "moe_fprop_pow2_16x16384"),
+    ("sweep", "quant_act_4096"),
+    ("sweep", "quant_act_16384"),
+    ("sweep", "quant_act_65536"),
+    ("sweep", "quant_act_pow2_4096"),
+    ("sweep", "quant_act_pow2_16384"),
+    ("sweep", "quant_act_pow2_65536"),
+    ("sweep", "quant_act_T_4096"),
+    ("sweep", "quant_act_T_16384"),
+    ("sweep", "quant_act_T_65536"),
+    ("sweep", "quant_act_T_pow2_65536"),
+    ("sweep", "quant_weight_7168x7168"),
+    ("sweep", "quant_weight_16x4096x7168"),
+    ("sweep", "square_2048"),
+    ("sweep", "square_4096"),
+    ("sweep", "square_8192"),
+    ("sweep", "square_16384"),
+]
 
 
 # ----------------------------------------------------------------- helpers
@@ -75,18 +116,22 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons, each stamped with
+    the host time it arrived, for the whole run; summary() picks the samples
+    of one timed window.  Query only: it changes no setting of the GPU."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int, period_ms: int = 100):
         self.gpu_index, self.period_ms = gpu_index, period_ms
         self.proc = None
-        self.lines = []
+        self.samples = []           # (host time, sm MHz, max MHz, power W, active reasons)
+        self.first = threading.Event()
 
-    def __enter__(self):
+    def start(self, wait_s: float = 5.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
@@ -94,15 +139,25 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            self.first.wait(wait_s)      # the first sample is in before timing starts
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, smax, pw = float(parts[1]), float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            act = [nm for nm, v in zip(self.REASONS, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, smax, pw, act))
+            self.first.set()
 
-    def __exit__(self, *exc):
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -110,27 +165,16 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.thread.join(timeout=5)
+            self.proc = None
 
-    def summary(self):
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+    def summary(self, t0: float, t1: float):
+        win = [s for s in list(self.samples) if t0 <= s[0] <= t1]
+        if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "power_w_max": max(power), "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(s[1] for s in win),
+                "sm_max_mhz": max(s[2] for s in win),
+                "power_w_max": max(s[3] for s in win),
+                "reasons": sorted({r for s in win for r in s[4]}), "samples": len(win)}
 
 
 def profile_traffic(kernel: str, workload: str):
@@ -169,25 +213,50 @@ def whole_job_value(work_per_rank, world, ms_step, scale):
     return world * work_per_rank / (ms_step * 1e-3) / scale
 
 
-def _pinned(bits):
+_HOST_CACHE = {}
+
+
+def cached(key, make):
+    """Host inputs drawn once per process (several workloads share a tensor)."""
+    if key not in _HOST_CACHE:
+        _HOST_CACHE[key] = make()
+    return _HOST_CACHE[key]
+
+
+def _host_tensor(bits, pin):
     import torch
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16) \
-        .pin_memory()
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory() if pin else t
 
 
-def _host_copies(inp, names, host):
-    """Pinned host copies of the named BF16 inputs (shared with `host` if given)."""
+def _host_copies(inp, names, host, pin=True):
+    """Host copies of the named BF16 inputs (shared with `host` if given);
+    pinned for the end-to-end leg."""
     if host is not None:
         return {n + "_h": host[n + "_h"] for n in names}
-    return {n + "_h": _pinned(inp[n]) for n in names}
+    return {n + "_h": _host_tensor(inp[n], pin) for n in names}
 
 
-def _pinned_out(host, name, shape, dtype):
-    """Pinned host buffer for a result (shared with `host`'s if given)."""
+def _host_out(host, name, shape, dtype, pin=True):
+    """Host buffer for a result (shared with `host`'s if given)."""
     import torch
     if host is not None:
         return host["io_out"][name][0]
-    return torch.empty(shape, dtype=dtype).pin_memory()
+    t = torch.empty(shape, dtype=dtype)
+    return t.pin_memory() if pin else t
+
+
+def _row_sample(M, n, seed=0):
+    return np.sort(np.random.default_rng(seed).choice(M, size=min(M, n), replace=False))
+
+
+def _rows_for_budget(run, M, budget_s):
+    """Rows of a seeded sample sized so that run(rows) takes about budget_s."""
+    probe = np.arange(min(M, 8))
+    t0 = time.perf_counter()
+    run(probe)
+    t_probe = max(time.perf_counter() - t0, 1e-3)
+    return int(min(M, max(probe.size, probe.size * max(budget_s, 0.25) / t_probe)))
 
 
 # ----------------------------------------------------------------- workloads
@@ -200,15 +269,33 @@ class Kernel:
 
 class Workload:
     unit = "TFLOP/s"
+    work_bound = "tensor"
+    io_inputs = ()
 
     def host_inputs(self):            # name -> BF16 bits / int arrays
         raise NotImplementedError
 
-    def setup(self, dev, inp):         # device tensors; pinned host copies
+    def setup(self, dev, inp, host=None, pin=True):   # device tensors; host copies
         raise NotImplementedError
 
     def kernels(self, st, stream):     # list of Kernel
         raise NotImplementedError
+
+    def cpu_step(self, inp, budget_s, full=False):
+        """The oracle on this step: every part in full when `full`, else a
+        bounded sample.  Returns a dict: est_s (time of the whole step,
+        extrapolated linearly where rows were sampled), spent (seconds
+        actually run), work_done (the metric's work of what was run), sample
+        (description), and the references kept for error reports."""
+        raise NotImplementedError
+
+    def work(self):
+        """Algorithmic work of one step in the metric's unit (same formulas
+        as kernels(); no GPU needed)."""
+        raise NotImplementedError
+
+    def in_bytes(self, inp):
+        return sum(int(inp[n].nbytes) for n in self.io_inputs)
 
     def h2d(self, st):                  # copy the step's inputs host -> device
         for name, (host, dev) in st["io_in"].items():
@@ -223,15 +310,12 @@ class Workload:
         bo = sum(h.numel() * h.element_size() for h, _ in st["io_out"].values())
         return bi, bo
 
-    def work_per_step(self, st, stream):
-        return sum(k.work for k in self.kernels(st, stream) if k.bound == self.work_bound)
-
-    work_bound = "tensor"
-
 
 class Fprop(Workload):
     """quant_act(X) + quant_weight(W) + GEMM.  pow2: power-of-two scales, and the
     GEMM on the block-scaled MMA (fp8q_gemm_pow2)."""
+
+    io_inputs = ("X", "W")
 
     def __init__(self, name, M, N, K, pow2=False):
         self.name, self.M, self.N, self.K, self.pow2 = name, M, N, K, pow2
@@ -242,14 +326,15 @@ class Fprop(Workload):
 
     def host_inputs(self):
         from fp8_fine_grained_amax_gb300 import synth
-        tag = self.name
-        return {"X": synth.activation(self.M, self.K, seed=0, name=f"{tag}.X"),
-                "W": synth.weight(self.N, self.K, seed=0, name=f"{tag}.W")}
+        tag = self.name.replace("_pow2", "")
+        M, N, K = self.M, self.N, self.K
+        return {"X": cached(("act", M, K, tag), lambda: synth.activation(M, K, 0, f"{tag}.X")),
+                "W": cached(("w", N, K, tag), lambda: synth.weight(N, K, 0, f"{tag}.W"))}
 
-    def setup(self, dev, inp, host=None):
+    def setup(self, dev, inp, host=None, pin=True):
         import torch
         M, N, K = self.M, self.N, self.K
-        st = _host_copies(inp, ("X", "W"), host)
+        st = _host_copies(inp, ("X", "W"), host, pin)
         st["X"], st["W"] = st["X_h"].to(dev), st["W_h"].to(dev)
         st["qa"] = torch.empty((M, K), dtype=torch.uint8, device=dev)
         st["sa"] = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
@@ -257,7 +342,7 @@ class Fprop(Workload):
         st["sb"] = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
         st["C"] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         st["io_in"] = {"X": (st["X_h"], st["X"]), "W": (st["W_h"], st["W"])}
-        st["io_out"] = {"C": (_pinned_out(host, "C", (M, N), torch.bfloat16), st["C"])}
+        st["io_out"] = {"C": (_host_out(host, "C", (M, N), torch.bfloat16, pin), st["C"])}
         return st
 
     def kernels(self, st, stream):
@@ -279,26 +364,42 @@ class Fprop(Workload):
                    2.0 * M * N * K, "tensor"),
         ]
 
-    def cpu_step(self, inp, target_s):
+    def work(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def cpu_step(self, inp, budget_s, full=False):
         import oracle
-        M, N, K = self.M, self.N, self.K
+        M, N, K, p2 = self.M, self.N, self.K, self.pow2
         t0 = time.perf_counter()
-        qa, sa = oracle.quant_act(inp["X"], self.pow2)
-        t_act = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        qb, sb = oracle.quant_weight(inp["W"], self.pow2)
+        qb, sb = oracle.quant_weight(inp["W"], p2)
         t_w = time.perf_counter() - t0
-        rows, t_g = _sampled_rows(
-            lambda r: oracle.gemm_rows(qa, sa, qb, sb, oracle.BSCALE_BLOCK, r), M,
-            target_s - t_act - t_w)
-        step_s = t_act + t_w + t_g * M / rows
-        return step_s, (f"quant_act {M}x{K} and quant_weight {N}x{K} in full "
-                        f"({t_act:.2f} s + {t_w:.2f} s); GEMM on {rows} of {M} rows "
-                        f"({t_g:.2f} s), extrapolated linearly to {M} rows"), t_act + t_w + t_g
+        if full:
+            rows = np.arange(M)
+        else:
+            def probe(r):
+                qa_r, sa_r = oracle.quant_act(inp["X"][r], p2)
+                oracle.gemm_rows(qa_r, sa_r, qb, sb, oracle.BSCALE_BLOCK)
+            rows = _row_sample(M, _rows_for_budget(probe, M, budget_s - t_w))
+        # the sampled rows' activations are quantised (1x128 tiles are per row)
+        t0 = time.perf_counter()
+        qa, sa = oracle.quant_act(np.ascontiguousarray(inp["X"][rows]), p2)
+        t_a = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        c_ref, absdot = oracle.gemm_rows(qa, sa, qb, sb, oracle.BSCALE_BLOCK)
+        t_g = time.perf_counter() - t0
+        r = rows.size
+        est = t_w + (t_a + t_g) * M / r
+        what = "in full" if r == M else f"on {r} of {M} rows, extrapolated linearly"
+        return {"est_s": est, "spent": t_w + t_a + t_g, "work_done": 2.0 * r * N * K,
+                "sample": (f"quant_weight {N}x{K} in full ({t_w:.2f} s); quant_act and GEMM "
+                           f"{what} ({t_a:.2f} s + {t_g:.2f} s)"),
+                "rows": rows, "c_ref": c_ref, "absdot": absdot}
 
 
 class LinearBwd(Workload):
     """Backward of Y = X W^T with X [T][d_in], W [d_out][d_in], dY [T][d_out]."""
+
+    io_inputs = ("dY", "X", "W")
 
     def __init__(self, T=8192, d_in=7168, d_out=2048, pow2=False):
         self.name = f"linear_bwd_pow2_T{T}" if pow2 else f"linear_bwd_T{T}"
@@ -312,25 +413,25 @@ class LinearBwd(Workload):
     def host_inputs(self):
         from fp8_fine_grained_amax_gb300 import synth
         T, di, do = self.T, self.d_in, self.d_out
-        return {"dY": synth.normal_bf16((T, do), 1e-3, 0, "bwd.dY"),
-                "X": synth.activation(T, di, seed=0, name="bwd.X"),
-                "W": synth.weight(do, di, seed=0, name="bwd.W")}
+        return {"dY": cached(("dY", T, do), lambda: synth.normal_bf16((T, do), 1e-3, 0, "bwd.dY")),
+                "X": cached(("bX", T, di), lambda: synth.activation(T, di, 0, "bwd.X")),
+                "W": cached(("bW", do, di), lambda: synth.weight(do, di, 0, "bwd.W"))}
 
-    def setup(self, dev, inp, host=None):
+    def setup(self, dev, inp, host=None, pin=True):
         import torch
         T, di, do = self.T, self.d_in, self.d_out
         u8, f32 = torch.uint8, torch.float32
-        st = _host_copies(inp, tuple(inp), host)
-        for k in inp:
+        st = _host_copies(inp, self.io_inputs, host, pin)
+        for k in self.io_inputs:
             st[k] = st[k + "_h"].to(dev)
         e = lambda *s, dt=u8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
         st.update(qdyT=e(do, T), sdyT=e(T // 128, do, dt=f32), qdy=e(T, do),
                   sdy=e(do // 128, T, dt=f32), qxT=e(di, T), sxT=e(T // 128, di, dt=f32),
                   qw=e(do, di), sw=e(do // 128, di // 128, dt=f32), qwT=e(di, do),
                   dX=e(T, di, dt=torch.bfloat16), dW=e(do, di, dt=f32))
-        st["io_in"] = {k: (st[k + "_h"], st[k]) for k in inp}
-        st["io_out"] = {"dX": (_pinned_out(host, "dX", (T, di), torch.bfloat16), st["dX"]),
-                        "dW": (_pinned_out(host, "dW", (do, di), f32), st["dW"])}
+        st["io_in"] = {k: (st[k + "_h"], st[k]) for k in self.io_inputs}
+        st["io_out"] = {"dX": (_host_out(host, "dX", (T, di), torch.bfloat16, pin), st["dX"]),
+                        "dW": (_host_out(host, "dW", (do, di), f32, pin), st["dW"])}
         return st
 
     def kernels(self, st, stream):
@@ -360,29 +461,82 @@ class LinearBwd(Workload):
                 "tensor"),
         ]
 
-    def cpu_step(self, inp, target_s):
+    def work(self):
+        return 2 * 2.0 * self.T * self.d_in * self.d_out
+
+    def _quantise(self, inp):
         import oracle
-        T, di, do = self.T, self.d_in, self.d_out
-        t0 = time.perf_counter()
         p2 = self.pow2
         qdyT, sdyT = oracle.quant_act_T(inp["dY"], p2)
         qdy, sdy = oracle.quant_act(inp["dY"], p2)
         qxT, sxT = oracle.quant_act_T(inp["X"], p2)
         qw, sw = oracle.quant_weight(inp["W"], p2)
-        qwT = np.ascontiguousarray(qw.T)
+        return qdyT, sdyT, qdy, sdy, qxT, sxT, np.ascontiguousarray(qw.T), sw
+
+    def cpu_step(self, inp, budget_s, full=False):
+        import oracle
+        T, di, do = self.T, self.d_in, self.d_out
+        t0 = time.perf_counter()
+        qdyT, sdyT, qdy, sdy, qxT, sxT, qwT, sw = self._quantise(inp)
         t_q = time.perf_counter() - t0
-        budget = (target_s - t_q) / 2
-        rd, t_d = _sampled_rows(lambda r: oracle.gemm_rows(qdy, sdy, qwT, sw,
-                                                           oracle.BSCALE_BLOCK_T, r), T, budget)
-        rw, t_w = _sampled_rows(lambda r: oracle.gemm_rows(qdyT, sdyT, qxT, sxT,
-                                                           oracle.BSCALE_ROW, r), do, budget)
-        step_s = t_q + t_d * T / rd + t_w * do / rw
-        return step_s, (f"all quantisers in full ({t_q:.2f} s); Dgrad on {rd} of {T} rows "
-                        f"({t_d:.2f} s) and Wgrad on {rw} of {do} rows ({t_w:.2f} s), "
-                        "extrapolated linearly"), t_q + t_d + t_w
+        dgrad = lambda r: oracle.gemm_rows(qdy, sdy, qwT, sw, oracle.BSCALE_BLOCK_T, r)  # noqa
+        wgrad = lambda r: oracle.gemm_rows(qdyT, sdyT, qxT, sxT, oracle.BSCALE_ROW, r)  # noqa
+        half = (budget_s - t_q) / 2
+        rd = np.arange(T) if full else _row_sample(T, _rows_for_budget(dgrad, T, half))
+        rw = np.arange(do) if full else _row_sample(do, _rows_for_budget(wgrad, do, half), 1)
+        t0 = time.perf_counter()
+        dgrad(rd)
+        t_d = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        wgrad(rw)
+        t_w = time.perf_counter() - t0
+        est = t_q + t_d * T / rd.size + t_w * do / rw.size
+        what = "in full" if (rd.size == T and rw.size == do) else \
+            f"on {rd.size} of {T} and {rw.size} of {do} rows, extrapolated linearly"
+        return {"est_s": est, "spent": t_q + t_d + t_w,
+                "work_done": 2.0 * di * (rd.size * do + rw.size * T),
+                "sample": (f"all quantisers in full ({t_q:.2f} s); Dgrad and Wgrad {what} "
+                           f"({t_d:.2f} s + {t_w:.2f} s)")}
+
+
+class LinearBwdCached(LinearBwd):
+    """The same backward, with X taken from the forward pass's FP8 cache (1x128
+    codes and scales) and requantised 128x1 instead of read again as BF16."""
+
+    def __init__(self, T=8192, d_in=7168, d_out=2048):
+        super().__init__(T, d_in, d_out)
+        self.name = f"linear_bwd_cached_T{T}"
+        self.config = dict(self.config, step="quant_act_T(dY, fused 1x128) + requant_act_T(X "
+                           "from FP8 cache) + quant_weight(W, transposed) + Dgrad + Wgrad")
+
+    def setup(self, dev, inp, host=None, pin=True):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        st = super().setup(dev, inp, host, pin)
+        st["qx_cache"], st["sx_cache"] = B.fp8q_quant_act(st["X"])   # the forward pass's cache
+        return st
+
+    def kernels(self, st, stream):
+        from fp8_fine_grained_amax_gb300 import binding as B
+        ks = super().kernels(st, stream)
+        T, di = self.T, self.d_in
+        ks[1] = Kernel("requant_act_T_kernel(X)", lambda: B.fp8q_requant_act_T(
+            st["qx_cache"], st["sx_cache"], qT=st["qxT"], sT=st["sxT"], stream=stream),
+            T * di * 2 + (di // 128) * T * 4 + (T // 128) * di * 4, "hbm")
+        return ks
+
+    def _quantise(self, inp):
+        import oracle
+        qx, sx = oracle.quant_act(inp["X"])    # the forward pass's cache
+        qdyT, sdyT = oracle.quant_act_T(inp["dY"])
+        qdy, sdy = oracle.quant_act(inp["dY"])
+        qxT, sxT = oracle.requant_act_T(qx, sx)
+        qw, sw = oracle.quant_weight(inp["W"])
+        return qdyT, sdyT, qdy, sdy, qxT, sxT, np.ascontiguousarray(qw.T), sw
 
 
 class MoEFprop(Workload):
+    io_inputs = ("X", "H", "Wup", "Wdown")
+
     def __init__(self, G=16, tokens=16384, d_model=7168, d_ff=4096, d_down_in=2048, pow2=False):
         self.name = f"moe_fprop_pow2_{G}x{tokens}" if pow2 else f"moe_fprop_{G}x{tokens}"
         self.pow2 = pow2
@@ -396,19 +550,21 @@ class MoEFprop(Workload):
 
     def host_inputs(self):
         from fp8_fine_grained_amax_gb300 import synth
-        G, T = self.G, self.T
+        G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
         return {"offs": synth.moe_offsets(T, G, 0.5, seed=0),
-                "X": synth.activation(T, self.dm, seed=0, name="moe.X"),
-                "H": synth.normal_bf16((T, self.ddi), 1.0, 0, "moe.H"),
-                "Wup": synth.weight(G * self.dff, self.dm, seed=0, name="moe.Wup"),
-                "Wdown": synth.weight(G * self.dm, self.ddi, seed=0, name="moe.Wdown")}
+                "X": cached(("moeX", T, dm), lambda: synth.activation(T, dm, 0, "moe.X")),
+                "H": cached(("moeH", T, ddi), lambda: synth.normal_bf16((T, ddi), 1.0, 0, "moe.H")),
+                "Wup": cached(("moeWup", G, dff, dm),
+                              lambda: synth.weight(G * dff, dm, 0, "moe.Wup")),
+                "Wdown": cached(("moeWdn", G, dm, ddi),
+                                lambda: synth.weight(G * dm, ddi, 0, "moe.Wdown"))}
 
-    def setup(self, dev, inp, host=None):
+    def setup(self, dev, inp, host=None, pin=True):
         import torch
         G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
         u8, f32 = torch.uint8, torch.float32
-        st = _host_copies(inp, ("X", "H", "Wup", "Wdown"), host)
-        for k in ("X", "H", "Wup", "Wdown"):
+        st = _host_copies(inp, self.io_inputs, host, pin)
+        for k in self.io_inputs:
             st[k] = st[k + "_h"].to(dev)
         st["offs"] = torch.from_numpy(inp["offs"]).to(dev)
         e = lambda *s, dt=u8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
@@ -416,9 +572,9 @@ class MoEFprop(Workload):
                   qup=e(G * dff, dm), sup=e(G * dff // 128, dm // 128, dt=f32),
                   qdn=e(G * dm, ddi), sdn=e(G * dm // 128, ddi // 128, dt=f32),
                   Yup=e(T, dff, dt=torch.bfloat16), Ydn=e(T, dm, dt=torch.bfloat16))
-        st["io_in"] = {k: (st[k + "_h"], st[k]) for k in ("X", "H", "Wup", "Wdown")}
-        st["io_out"] = {"Yup": (_pinned_out(host, "Yup", (T, dff), torch.bfloat16), st["Yup"]),
-                        "Ydn": (_pinned_out(host, "Ydn", (T, dm), torch.bfloat16), st["Ydn"])}
+        st["io_in"] = {k: (st[k + "_h"], st[k]) for k in self.io_inputs}
+        st["io_out"] = {"Yup": (_host_out(host, "Yup", (T, dff), torch.bfloat16, pin), st["Yup"]),
+                        "Ydn": (_host_out(host, "Ydn", (T, dm), torch.bfloat16, pin), st["Ydn"])}
         return st
 
     def kernels(self, st, stream):
@@ -450,98 +606,74 @@ class MoEFprop(Workload):
                 stream=stream), 2.0 * T * dm * ddi, "tensor"),
         ]
 
-    def cpu_step(self, inp, target_s):
+    def work(self):
+        return 2.0 * self.T * self.dff * self.dm + 2.0 * self.T * self.dm * self.ddi
+
+    def cpu_step(self, inp, budget_s, full=False):
         import oracle
-        G, T, dm, dff, ddi = self.G, self.T, self.dm, self.dff, self.ddi
+        G, T, dm, dff, ddi, p2 = self.G, self.T, self.dm, self.dff, self.ddi, self.pow2
         t0 = time.perf_counter()
-        p2 = self.pow2
-        qx, sx = oracle.quant_act(inp["X"], p2)
-        qh, sh = oracle.quant_act(inp["H"], p2)
         qup, sup = oracle.quant_weight(inp["Wup"], p2)
         qdn, sdn = oracle.quant_weight(inp["Wdown"], p2)
-        t_q = time.perf_counter() - t0
-        budget = (target_s - t_q) / 2
+        t_w = time.perf_counter() - t0
         offs = inp["offs"]
-        ru, t_u = _sampled_rows(lambda r: oracle.grouped_gemm_rows(
-            qx, sx, qup.reshape(G, dff, dm), sup.reshape(G, dff // 128, dm // 128), offs, r),
-            T, budget)
-        rd, t_d = _sampled_rows(lambda r: oracle.grouped_gemm_rows(
-            qh, sh, qdn.reshape(G, dm, ddi), sdn.reshape(G, dm // 128, ddi // 128), offs, r),
-            T, budget)
-        step_s = t_q + t_u * T / ru + t_d * T / rd
-        return step_s, (f"all quantisers in full ({t_q:.2f} s); grouped GEMMs on {ru} and {rd} "
-                        f"of {T} rows ({t_u:.2f} s, {t_d:.2f} s), extrapolated linearly"), \
-            t_q + t_u + t_d
+        qup, sup = qup.reshape(G, dff, dm), sup.reshape(G, dff // 128, dm // 128)
+        qdn, sdn = qdn.reshape(G, dm, ddi), sdn.reshape(G, dm // 128, ddi // 128)
 
+        def part(x, qb, sb, rows):   # the listed tokens' 1x128 tiles and GEMM rows
+            qa, sa = oracle.quant_act(np.ascontiguousarray(x[rows]), p2)
+            # each sampled token keeps its expert: offsets of the sample
+            g_of = np.searchsorted(offs, rows, side="right") - 1
+            o = np.zeros(G + 1, np.int32)
+            o[1:] = np.cumsum(np.bincount(g_of, minlength=G))
+            oracle.grouped_gemm_rows(qa, sa, qb, sb, o)
 
-class LinearBwdCached(LinearBwd):
-    """The same backward, with X taken from the forward pass's FP8 cache (1x128
-    codes and scales) and requantised 128x1 instead of read again as BF16."""
-
-    def __init__(self, T=8192, d_in=7168, d_out=2048):
-        super().__init__(T, d_in, d_out)
-        self.name = f"linear_bwd_cached_T{T}"
-        self.config = dict(self.config, step="quant_act_T(dY, fused 1x128) + requant_act_T(X "
-                           "from FP8 cache) + quant_weight(W, transposed) + Dgrad + Wgrad")
-
-    def setup(self, dev, inp, host=None):
-        from fp8_fine_grained_amax_gb300 import binding as B
-        st = super().setup(dev, inp, host)
-        st["qx_cache"], st["sx_cache"] = B.fp8q_quant_act(st["X"])   # the forward pass's cache
-        return st
-
-    def kernels(self, st, stream):
-        from fp8_fine_grained_amax_gb300 import binding as B
-        ks = super().kernels(st, stream)
-        T, di = self.T, self.d_in
-        ks[1] = Kernel("requant_act_T_kernel(X)", lambda: B.fp8q_requant_act_T(
-            st["qx_cache"], st["sx_cache"], qT=st["qxT"], sT=st["sxT"], stream=stream),
-            T * di * 2 + (di // 128) * T * 4 + (T // 128) * di * 4, "hbm")
-        return ks
-
-    def cpu_step(self, inp, target_s):
-        import oracle
-        T, di, do = self.T, self.d_in, self.d_out
-        qx, sx = oracle.quant_act(inp["X"])          # the forward pass's cache (not timed)
+        half = (budget_s - t_w) / 2
+        ru = np.arange(T) if full else _row_sample(
+            T, _rows_for_budget(lambda r: part(inp["X"], qup, sup, r), T, half))
+        rd = np.arange(T) if full else _row_sample(
+            T, _rows_for_budget(lambda r: part(inp["H"], qdn, sdn, r), T, half), 1)
         t0 = time.perf_counter()
-        qdyT, sdyT = oracle.quant_act_T(inp["dY"])
-        qdy, sdy = oracle.quant_act(inp["dY"])
-        qxT, sxT = oracle.requant_act_T(qx, sx)
-        qw, sw = oracle.quant_weight(inp["W"])
-        qwT = np.ascontiguousarray(qw.T)
-        t_q = time.perf_counter() - t0
-        budget = (target_s - t_q) / 2
-        rd, t_d = _sampled_rows(lambda r: oracle.gemm_rows(qdy, sdy, qwT, sw,
-                                                           oracle.BSCALE_BLOCK_T, r), T, budget)
-        rw, t_w = _sampled_rows(lambda r: oracle.gemm_rows(qdyT, sdyT, qxT, sxT,
-                                                           oracle.BSCALE_ROW, r), do, budget)
-        step_s = t_q + t_d * T / rd + t_w * do / rw
-        return step_s, (f"all quantisers in full ({t_q:.2f} s); Dgrad on {rd} of {T} rows "
-                        f"({t_d:.2f} s) and Wgrad on {rw} of {do} rows ({t_w:.2f} s), "
-                        "extrapolated linearly"), t_q + t_d + t_w
+        part(inp["X"], qup, sup, ru)
+        t_u = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        part(inp["H"], qdn, sdn, rd)
+        t_d = time.perf_counter() - t0
+        est = t_w + t_u * T / ru.size + t_d * T / rd.size
+        what = "in full" if ru.size == T and rd.size == T else \
+            f"on {ru.size} and {rd.size} of {T} tokens, extrapolated linearly"
+        return {"est_s": est, "spent": t_w + t_u + t_d,
+                "work_done": 2.0 * ru.size * dff * dm + 2.0 * rd.size * dm * ddi,
+                "sample": (f"expert weights quantised in full ({t_w:.2f} s); token quantisation "
+                           f"and grouped GEMMs {what} ({t_u:.2f} s + {t_d:.2f} s)")}
 
 
 class QuantOnly(Workload):
     unit = "GB/s"
     work_bound = "hbm"
+    io_inputs = ("X",)
 
-    def __init__(self, kind, rows, cols=7168):
-        self.kind, self.rows, self.cols = kind, rows, cols
-        self.name = f"{kind}_{rows}" if kind != "quant_weight" else f"quant_weight_{rows // 4096}x4096"
-        self.config = {"rows": rows, "cols": cols, "step": kind}
+    def __init__(self, name, kind, rows, cols=7168, groups=1):
+        self.kind, self.rows, self.cols, self.groups = kind, rows, cols, groups
+        self.name = name
+        self.config = {"rows": rows * groups, "cols": cols, "step": kind}
+        if groups > 1:
+            self.config["weights"] = f"{groups} x {rows}x{cols}"
 
     def host_inputs(self):
         from fp8_fine_grained_amax_gb300 import synth
+        R, C = self.rows * self.groups, self.cols
         if self.kind == "quant_weight":
-            return {"X": synth.weight(self.rows, self.cols, seed=0, name=f"sweep.W{self.rows}")}
-        return {"X": synth.activation(self.rows, self.cols, seed=0, name=f"sweep.X{self.rows}")}
+            return {"X": cached(("sweepW", R, C), lambda: synth.weight(R, C, 0, f"sweep.W{R}"))}
+        return {"X": cached(("sweepX", R, C),
+                            lambda: synth.activation(R, C, 0, f"sweep.X{R}"))}
 
-    def setup(self, dev, inp, host=None):
+    def setup(self, dev, inp, host=None, pin=True):
         import torch
-        R, C = self.rows, self.cols
-        st = _host_copies(inp, ("X",), host)
+        R, C = self.rows * self.groups, self.cols
+        st = _host_copies(inp, ("X",), host, pin)
         st["X"] = st["X_h"].to(dev)
-        if self.kind == "quant_act_T":
+        if self.kind.startswith("quant_act_T"):
             st["q"] = torch.empty((C, R), dtype=torch.uint8, device=dev)
             st["s"] = torch.empty((R // 128, C), dtype=torch.float32, device=dev)
         elif self.kind == "quant_weight":
@@ -551,18 +683,21 @@ class QuantOnly(Workload):
             st["q"] = torch.empty((R, C), dtype=torch.uint8, device=dev)
             st["s"] = torch.empty((C // 128, R), dtype=torch.float32, device=dev)
         st["io_in"] = {"X": (st["X_h"], st["X"])}
-        st["io_out"] = {"q": (_pinned_out(host, "q", tuple(st["q"].shape), torch.uint8), st["q"])}
+        st["io_out"] = {"q": (_host_out(host, "q", tuple(st["q"].shape), torch.uint8, pin),
+                              st["q"])}
         return st
 
     def kernels(self, st, stream):
         from fp8_fine_grained_amax_gb300 import binding as B
-        R, C = self.rows, self.cols
-        if self.kind == "quant_act_T":
+        R, C = self.rows * self.groups, self.cols
+        if self.kind.startswith("quant_act_T"):
+            mode = B.FP8Q_SCALE_POW2 if self.kind == "quant_act_T_pow2" else B.FP8Q_SCALE_FP32
             return [Kernel("quant_act_T_kernel", lambda: B.fp8q_quant_act_T(
-                st["X"], qT=st["q"], sT=st["s"], stream=stream), R * C * 3 + R * C // 32, "hbm")]
+                st["X"], qT=st["q"], sT=st["s"], scale_mode=mode, stream=stream),
+                R * C * 3 + R * C // 32, "hbm")]
         if self.kind == "quant_weight":
             return [Kernel("quant_weight_kernel", lambda: B.fp8q_quant_weight(
-                st["X"], q=st["q"], sb=st["s"], stream=stream), R * C * 3, "hbm")]
+                st["X"], q=st["q"], sb=st["s"], stream=stream), self.work(), "hbm")]
         if self.kind == "quant_tensor":
             if "ws" not in st:
                 import torch
@@ -577,32 +712,28 @@ class QuantOnly(Workload):
             st["X"], q=st["q"], sa=st["s"], scale_mode=mode, stream=stream),
             R * C * 3 + R * C // 32, "hbm")]
 
-    def cpu_step(self, inp, target_s):
+    def work(self):
+        R, C = self.rows * self.groups, self.cols
+        if self.kind == "quant_weight":
+            return R * C * 3 + ((R + 127) // 128) * (C // 128) * 4
+        return R * C * 3 + (0 if self.kind == "quant_tensor" else R * C // 32)
+
+    def cpu_step(self, inp, budget_s, full=False):
         import oracle
         t0 = time.perf_counter()
-        if self.kind == "quant_act_T":
-            oracle.quant_act_T(inp["X"])
+        p2 = self.kind.endswith("_pow2")
+        if self.kind.startswith("quant_act_T"):
+            oracle.quant_act_T(inp["X"], p2)
         elif self.kind == "quant_tensor":
             oracle.quant_tensor(inp["X"])
         elif self.kind == "quant_weight":
             oracle.quant_weight(inp["X"])
         else:
-            oracle.quant_act(inp["X"], self.kind == "quant_act_pow2")
+            oracle.quant_act(inp["X"], p2)
         t = time.perf_counter() - t0
-        return t, f"{self.kind} on the full {self.rows}x{self.cols} input ({t:.2f} s)", t
-
-
-def _sampled_rows(run, M, budget_s):
-    """Time `run(rows)` on a seeded row sample sized to about budget_s seconds."""
-    rows = min(M, 8)
-    t0 = time.perf_counter()
-    run(np.arange(rows))
-    t_probe = time.perf_counter() - t0
-    n = int(min(M, max(rows, rows * max(budget_s, 0.5) / max(t_probe, 1e-3))))
-    sample = np.sort(np.random.default_rng(0).choice(M, size=n, replace=False))
-    t0 = time.perf_counter()
-    run(sample)
-    return n, time.perf_counter() - t0
+        return {"est_s": t, "spent": t, "work_done": self.work(),
+                "sample": f"{self.kind} on the full {self.rows * self.groups}x{self.cols} "
+                          f"input ({t:.2f} s)"}
 
 
 def make_workload(name: str) -> Workload:
@@ -610,8 +741,6 @@ def make_workload(name: str) -> Workload:
         return Fprop(name, 4096, 7168, 7168)
     if name == "fprop_pow2_4096x7168x7168":
         return Fprop(name, 4096, 7168, 7168, pow2=True)
-    if name == "linear_bwd_pow2_T8192":
-        return LinearBwd(pow2=True)
     if name == "tiny_fprop":
         return Fprop(name, 256, 256, 512)
     if name.startswith("square_"):
@@ -619,33 +748,205 @@ def make_workload(name: str) -> Workload:
         return Fprop(name, n, n, n)
     if name == "linear_bwd_T8192":
         return LinearBwd()
+    if name == "linear_bwd_pow2_T8192":
+        return LinearBwd(pow2=True)
+    if name == "linear_bwd_cached_T8192":
+        return LinearBwdCached()
     if name == "moe_fprop_16x16384":
         return MoEFprop()
     if name == "moe_fprop_pow2_16x16384":
         return MoEFprop(pow2=True)
-    if name == "linear_bwd_cached_T8192":
-        return LinearBwdCached()
-    for kind in ("quant_act_pow2", "quant_act_T", "quant_tensor", "quant_act"):
-        if name.startswith(kind + "_"):
-            return QuantOnly(kind, int(name[len(kind) + 1:]))
-    if name.startswith("quant_weight_") and name.endswith("x4096"):
-        return QuantOnly("quant_weight", int(name[len("quant_weight_"):-len("x4096")]) * 4096)
+    m = re.fullmatch(r"quant_weight_(\d+)x(\d+)(?:x(\d+))?", name)
+    if m:
+        a, b, c = int(m.group(1)), int(m.group(2)), m.group(3)
+        if c is not None:                      # g stacked n x k weights
+            return QuantOnly(name, "quant_weight", b, int(c), groups=a)
+        if b == 4096:                          # g stacked 4096 x 7168 weights
+            return QuantOnly(name, "quant_weight", 4096, 7168, groups=a)
+        return QuantOnly(name, "quant_weight", a, b)
+    for kind in ("quant_act_T_pow2", "quant_act_pow2", "quant_act_T", "quant_tensor", "quant_act"):
+        m = re.fullmatch(kind + r"_(\d+)", name)
+        if m:
+            return QuantOnly(name, kind, int(m.group(1)))
     raise SystemExit(f"unknown workload {name}")
 
 
-def cpu_baseline(wl: Workload, inp, target_s: float):
-    """The oracle, as it stands, on a bounded sample of one step; extrapolated
-    to the full step and reported in the metric's unit."""
+def workload_config(wl: Workload, in_bytes: int, world: int):
+    """The line's `config`: the same dict for both arms of one workload."""
+    l2 = (f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step > "
+          f"{L2_BYTES / 1e6:.0f} MB); no flush" if in_bytes > L2_BYTES else
+          f"inputs {in_bytes / 1e6:.0f} MB fit in L2: a {2 * L2_BYTES / 1e6:.0f} MB buffer is "
+          "overwritten before every step, outside the kernels' event span")
+    return dict(workload=wl.name, **wl.config, l2=l2, parallelism=f"replicas x{world}")
+
+
+def cpu_baseline(wl: Workload, inp, budget_s: float, full: bool):
+    """The oracle, as it stands, on one step (every part in full when `full`,
+    else a bounded sample extrapolated to the full step), in the metric's unit."""
     import oracle
-    step_s, sample, spent = wl.cpu_step(inp, target_s)
-    work = wl.cpu_work
+    r = wl.cpu_step(inp, budget_s, full)
     scale = 1e12 if wl.unit == "TFLOP/s" else 1e9
-    return {"value": round(work / step_s / scale, 6), "unit": wl.unit,
-            "cores": oracle.num_threads(), "kind": "oracle", "sample": sample,
-            "seconds": round(spent, 2)}
+    return {"value": round(wl.work() / r["est_s"] / scale, 6), "unit": wl.unit,
+            "cores": oracle.num_threads(), "kind": "oracle", "sample": r["sample"],
+            "seconds": round(r["spent"], 2)}, r
+
+
+def gemm_errors(wl: Fprop, inp, st, ref):
+    """Error of the GPU result on the oracle's rows: the largest
+    |C - C_ref| / tolerance, and (context) the relative Frobenius error
+    against an unquantised BF16 GEMM on a 256-row sample of them."""
+    import oracle
+    rows = ref["rows"]
+    c = st["C"].float().cpu().numpy().astype(np.float64)[rows]
+    tol = oracle.gemm_tolerance(ref["c_ref"], ref["absdot"], True)
+    ratio = float(np.max(np.abs(c - ref["c_ref"]) / tol))
+    sub = np.arange(rows.size) if rows.size <= 256 else _row_sample(rows.size, 256, 2)
+    c16 = oracle.bf16_gemm_rows(inp["X"], inp["W"], rows[sub])
+    fro = float(np.linalg.norm(c[sub] - c16) / np.linalg.norm(c16))
+    fro_q = float(np.linalg.norm(ref["c_ref"][sub] - c16) / np.linalg.norm(c16))
+    return {"rows_checked": int(rows.size), "cols": int(c.shape[1]),
+            "max_err_over_tol": round(ratio, 4),
+            "tolerance": "|C - C_ref| <= 2e-4 * sum_k |a_k b_k| + 0.5 ulp_bf16",
+            "rel_fro_err_vs_bf16_gemm": round(fro, 6),
+            "rel_fro_err_vs_bf16_gemm_oracle": round(fro_q, 6),
+            "bf16_rows": int(sub.size)}
 
 
 # ----------------------------------------------------------------- our arm
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class Timer:
+    """The K-step loop of one workload, with CUDA events between its kernels,
+    repeated `repeats` times; each repeat sits between a barrier and a device
+    synchronise.  With `flush`, every step first overwrites a buffer larger
+    than L2 (outside the events), so that a workload whose inputs would fit
+    in L2 reads them from HBM; its step time is then the span of its own
+    kernels, first event to last."""
+
+    def __init__(self, ks, stream, dev, steps, flush=False):
+        import torch
+        self.ks, self.stream, self.dev, self.steps = ks, stream, dev, steps
+        self.evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ks) + 1)]
+                    for _ in range(steps)]
+        self.e0 = torch.cuda.Event(enable_timing=True)
+        self.e1 = torch.cuda.Event(enable_timing=True)
+        self.flush_buf = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+                          if flush else None)
+
+    def step(self, ev=None):
+        if self.flush_buf is not None:
+            self.flush_buf.fill_(0x5A)
+        for i, k in enumerate(self.ks):
+            if ev is not None:
+                ev[i].record(self.stream)
+            k.fn()
+        if ev is not None:
+            ev[len(self.ks)].record(self.stream)
+
+    def run(self, repeats, world):
+        import torch
+        rep_ms, ksum, spans = [], [0.0] * len(self.ks), []
+        t0 = time.time()
+        for _ in range(repeats):
+            _barrier(world)
+            torch.cuda.synchronize(self.dev)
+            self.e0.record(self.stream)
+            for i in range(self.steps):
+                self.step(self.evs[i])
+            self.e1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            _barrier(world)
+            rep_ms.append(self.e0.elapsed_time(self.e1))
+            for ev in self.evs:
+                for i in range(len(self.ks)):
+                    ksum[i] += ev[i].elapsed_time(ev[i + 1])
+                if self.flush_buf is not None:
+                    spans.append(ev[0].elapsed_time(ev[len(self.ks)]))
+        t1 = time.time()
+        n = repeats * self.steps
+        ms_step = (statistics.median(spans) if spans else statistics.median(rep_ms) / self.steps)
+        return {"ms_step": ms_step, "kernel_ms": [s / n for s in ksum], "t0": t0, "t1": t1,
+                "timed_s": (sum(spans) if spans else sum(rep_ms)) / 1e3}
+
+
+def needs_flush(wl, inp):
+    """A step whose inputs fit in L2 gets an L2 flush before it."""
+    return wl.in_bytes(inp) <= L2_BYTES
+
+
+def repeats_for(per_step_s, steps, min_s, world, dev):
+    """Repeats of the K-step loop that make the timed region last min_s
+    (the same on every rank)."""
+    r = max(1, math.ceil(min_s / max(per_step_s * steps, 1e-6)))
+    r = min(r, 100000)
+    return int(max_over_ranks([r], world, device=dev)[0])
+
+
+def warm_up(timer, warmup, dev):
+    """W untimed steps, then one calibration pass of the K-step loop; returns
+    its device time per step (what sizes the repeats of the timed region)."""
+    import torch
+    for _ in range(warmup):
+        timer.step()
+    torch.cuda.synchronize(dev)
+    timer.e0.record(timer.stream)
+    for i in range(timer.steps):
+        timer.step(timer.evs[i])
+    timer.e1.record(timer.stream)
+    torch.cuda.synchronize(dev)
+    if timer.flush_buf is not None:   # the kernels' span, as the timed region counts it
+        return statistics.median(ev[0].elapsed_time(ev[len(timer.ks)])
+                                 for ev in timer.evs) * 1e-3
+    return timer.e0.elapsed_time(timer.e1) * 1e-3 / timer.steps
+
+
+def kernel_table(ks, kms, hbm, fp8_peak):
+    out = {}
+    for k, ms in zip(ks, kms):
+        if k.bound == "tensor":
+            a = k.work / (ms * 1e-3) / 1e12
+            out[k.name] = {"ms": round(ms, 5), "tflops": round(a, 1),
+                           "frac_fp8_peak": round(a / fp8_peak, 4)}
+        else:
+            a = k.work / (ms * 1e-3) / 1e9
+            out[k.name] = {"ms": round(ms, 5), "gbs": round(a, 1), "frac_hbm": round(a / hbm, 4)}
+    return out
+
+
+def measure_other(name, dev, stream, args, clk, hbm, fp8_peak):
+    """One more workload on this GPU: per-kernel times over a timed region of
+    at least --min-seconds, and the clocks seen during it."""
+    import torch
+    from fp8_fine_grained_amax_gb300 import binding as B
+    wl = make_workload(name)
+    inp = wl.host_inputs()
+    st = wl.setup(dev, inp, pin=False)
+    ks = wl.kernels(st, stream)
+    timer = Timer(ks, stream, dev, args.steps, flush=needs_flush(wl, inp))
+    per_step = warm_up(timer, args.warmup, dev)
+    if B.fp8q_sync_status(stream) != 0:
+        raise SystemExit(f"device status error in the warm-up of {name}")
+    reps = repeats_for(per_step, args.steps, args.min_seconds, 1, dev)
+    r = timer.run(reps, 1)
+    if B.fp8q_sync_status(stream) != 0:
+        raise SystemExit(f"device status error in {name}")
+    scale = 1e12 if wl.unit == "TFLOP/s" else 1e9
+    work = sum(k.work for k in ks if k.bound == wl.work_bound)
+    res = {"value": round(work / (r["ms_step"] * 1e-3) / scale, 2), "unit": wl.unit,
+           "ms_per_step": round(r["ms_step"], 5), "steps": args.steps, "repeats": reps,
+           "timed_s": round(r["timed_s"], 3),
+           "config": workload_config(wl, wl.in_bytes(inp), 1),
+           "kernels": kernel_table(ks, r["kernel_ms"], hbm, fp8_peak),
+           "clocks": clk.summary(r["t0"], r["t1"])}
+    del st, ks, timer
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local):
     import torch
     import torch.distributed as dist
@@ -659,50 +960,26 @@ def run_ours(args, rank, world, local):
     if rank == 0:
         from fp8_fine_grained_amax_gb300.build import build_library
         build_library()
-    if world > 1:
-        dist.barrier()
+    _barrier(world)
     B.load_library()
 
+    clk = ClockSampler(local).start()
     wl = make_workload(args.workload)
     inp = wl.host_inputs()
     st = wl.setup(dev, inp)
     stream = torch.cuda.current_stream(dev)
     ks = wl.kernels(st, stream)
+    timer = Timer(ks, stream, dev, args.steps, flush=needs_flush(wl, inp))
 
-    def step(ev=None):
-        for i, k in enumerate(ks):
-            if ev is not None:
-                ev[i].record(stream)
-            k.fn()
-        if ev is not None:
-            ev[len(ks)].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+    per_step = warm_up(timer, args.warmup, dev)
     if B.fp8q_sync_status(stream) != 0:
         raise SystemExit("device status error during warm-up")
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ks) + 1)]
-           for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
+    reps = repeats_for(per_step, args.steps, args.min_seconds, world, dev)
+    r = timer.run(reps, world)
     status = B.fp8q_sync_status(stream)
     if status != 0:
         raise SystemExit(f"device status {status} after the timed region")
-    kms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(len(ks))]
+    clocks = clk.summary(r["t0"], r["t1"])
 
     # end to end through host buffers: every step copies its inputs from pinned
     # host memory (H2D stream), runs its kernels (compute stream) and reads its
@@ -750,10 +1027,14 @@ def run_ours(args, rank, world, local):
     e2e_ms = e2e_run(e2e_steps) / e2e_steps
     if B.fp8q_sync_status(stream) != 0:
         raise SystemExit("device status error in the end-to-end leg")
+    # the timed steps ran on `st`; run one more step on it so that its output
+    # is this step's result again (the end-to-end leg reused its buffers)
+    timer.step()
+    torch.cuda.synchronize(dev)
 
-    ms_step = total_ms / args.steps
-    ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], world, device=dev)
+    ms_step, e2e_ms = max_over_ranks([r["ms_step"], e2e_ms], world, device=dev)
     if rank != 0:
+        clk.stop()
         if world > 1:
             dist.destroy_process_group()
         return None
@@ -762,16 +1043,8 @@ def run_ours(args, rank, world, local):
     fp8_peak = bf16 * FP8_OVER_BF16
     scale = 1e12 if wl.unit == "TFLOP/s" else 1e9
     work = sum(k.work for k in ks if k.bound == wl.work_bound)
-    kernels = {}
-    for k, ms in zip(ks, kms):
-        if k.bound == "tensor":
-            a = k.work / (ms * 1e-3) / 1e12
-            kernels[k.name] = {"ms": round(ms, 5), "tflops": round(a, 1),
-                               "frac_fp8_peak": round(a / fp8_peak, 4)}
-        else:
-            a = k.work / (ms * 1e-3) / 1e9
-            kernels[k.name] = {"ms": round(ms, 5), "gbs": round(a, 1),
-                               "frac_hbm": round(a / hbm, 4)}
+    kms = r["kernel_ms"]
+    kernels = kernel_table(ks, kms, hbm, fp8_peak)
     dom_i = max(range(len(ks)), key=lambda i: kms[i])
     dom = ks[dom_i]
     base_name = dom.name.split("(")[0]
@@ -788,7 +1061,6 @@ def run_ours(args, rank, world, local):
     roof["traffic"] = profile_traffic(base_name, wl.name)
     roof["kernel"] = dom.name
     roof["work_per_launch"] = dom.work
-    in_bytes = sum(h.numel() * h.element_size() for h, _ in st["io_in"].values())
     bi, bo = wl.io_bytes(st)
     line = {
         "metric": METRIC,
@@ -797,17 +1069,15 @@ def run_ours(args, rank, world, local):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
+        "repeats": reps,
+        "timed_s": round(r["timed_s"], 3),
         "ms_per_step": round(ms_step, 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "fp8_e4m3 (fp32 accumulate)" if wl.unit == "TFLOP/s" else "bf16 -> e4m3",
         "data": "synthetic",
-        "config": dict(workload=wl.name, **wl.config,
-                       l2=f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step > "
-                          f"{L2_BYTES / 1e6:.0f} MB); no flush" if in_bytes > L2_BYTES else
-                          f"inputs {in_bytes / 1e6:.0f} MB fit in L2; no flush",
-                       parallelism=f"replicas x{world}"),
+        "config": workload_config(wl, wl.in_bytes(inp), world),
         "roofline": roof,
         "kernels": dict(kernels, hbm_peak_gbs=hbm, fp8_peak_tflops=round(fp8_peak, 1),
                         peak_source=src),
@@ -815,12 +1085,24 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "pipeline": "H2D(i+1) and D2H(i-1) overlap kernels(i); 2 device buffer sets"},
-        "gpu_launches": len(ks) * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": len(ks) * args.steps * reps,
+        "clocks": clocks,
     }
     if not args.no_cpu_baseline:
-        wl.cpu_work = work
-        line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+        full = isinstance(wl, (Fprop, LinearBwd)) and wl.work() <= 1e12
+        cb, ref = cpu_baseline(wl, inp, args.cpu_seconds, full)
+        line["cpu_baseline"] = cb
+        if isinstance(wl, Fprop):
+            line["errors"] = gemm_errors(wl, inp, st, ref)
+    if world == 1 and args.all_workloads:
+        del st, st2, sets, ks, timer
+        torch.cuda.empty_cache()
+        others = {}
+        for _, name in CONFIG_WORKLOADS:
+            if name != wl.name:
+                others[name] = measure_other(name, dev, stream, args, clk, hbm, fp8_peak)
+        line["workloads"] = others
+    clk.stop()
     if world > 1:
         dist.destroy_process_group()
     return line
@@ -828,59 +1110,61 @@ def run_ours(args, rank, world, local):
 
 # ----------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
-    """Reference arm: the CPU oracle on the host cores, same metric and config."""
+    """Reference arm: the CPU oracle on the host cores, same metric and config.
+    Each step is a bounded sample of the workload's step (rows of its GEMMs;
+    quantisers whole or on the same rows); `value` is the work that sample did
+    per second it ran, `ms_per_step` the time one sampled step took."""
     if rank != 0:
         return None
+    import oracle
     wl = make_workload(args.workload)
     inp = wl.host_inputs()
-    wl.cpu_work = _work_of(wl)
-    per_step = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    vals = []
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    runs = []
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(wl, inp, per_step)
+        r = wl.cpu_step(inp, per_step, full=False)
         if i >= args.warmup:
-            vals.append(cb)
-    value = statistics.median(v["value"] for v in vals)
+            runs.append(r)
     scale = 1e12 if wl.unit == "TFLOP/s" else 1e9
-    cb = dict(vals[-1])
-    cb["value"] = value
+    rates = [r["work_done"] / r["spent"] / scale for r in runs]
+    value = round(statistics.median(rates), 6)
+    ms = statistics.median(r["spent"] for r in runs) * 1e3
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": wl.unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(wl.cpu_work / (value * scale) * 1e3, 3),
+        "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": dict(workload=wl.name, **wl.config, implementation="CPU oracle"),
-        "cpu_baseline": cb,
+        "config": workload_config(wl, wl.in_bytes(inp), world),
+        "work_per_step": runs[-1]["work_done"],
+        "cpu_baseline": {"value": value, "unit": wl.unit, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": "each step: " + runs[-1]["sample"]},
         "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 
 
-def _work_of(wl: Workload) -> float:
-    """Algorithmic work of one step without a GPU (same formulas as kernels())."""
-    if isinstance(wl, Fprop):
-        return 2.0 * wl.M * wl.N * wl.K
-    if isinstance(wl, LinearBwd):
-        return 2 * 2.0 * wl.T * wl.d_in * wl.d_out
-    if isinstance(wl, MoEFprop):
-        return 2.0 * wl.T * wl.dff * wl.dm + 2.0 * wl.T * wl.dm * wl.ddi
-    R, C = wl.rows, wl.cols
-    return R * C * 3 + (0 if wl.kind in ("quant_weight", "quant_tensor") else R * C // 32)
-
-
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="fprop_4096x7168x7168")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="shortest timed region per workload (repeats of the K-step loop)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-workloads", dest="all_workloads", action="store_true", default=None,
+                    help="also measure every other configuration's workloads (default: on for "
+                         "the headline workload on one GPU)")
+    ap.add_argument("--no-all-workloads", dest="all_workloads", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.all_workloads is None:
+        args.all_workloads = args.workload == HEADLINE
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, rank, world)

@@ -21,7 +21,9 @@ BF16 tensors are returned as numpy ``uint16`` bit patterns.
 """
 from __future__ import annotations
 
+import os
 import zlib
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -47,7 +49,9 @@ def normal_bf16(shape, std: float, seed: int, name: str,
     n = int(np.prod(shape)) if shape else 1
     out = np.empty(n, np.uint16)
     sid = stream_id(name)
-    for ci, lo in enumerate(range(0, n, CHUNK)):
+
+    def fill(ci: int) -> None:
+        lo = ci * CHUNK
         hi = min(n, lo + CHUNK)
         rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, sid, ci])))
         v = rng.standard_normal(hi - lo, dtype=np.float32)
@@ -56,6 +60,16 @@ def normal_bf16(shape, std: float, seed: int, name: str,
             u = rng.random(hi - lo, dtype=np.float32)
             v[u < np.float32(outlier_frac)] *= np.float32(outlier_mult)
         out[lo:hi] = _round_bf16(v)
+
+    # chunks are seeded independently, so drawing them on several threads
+    # (numpy releases the GIL while it fills and rounds) gives the same bytes
+    n_chunks = (n + CHUNK - 1) // CHUNK
+    if n_chunks <= 2:
+        for ci in range(n_chunks):
+            fill(ci)
+    else:
+        with ThreadPoolExecutor(min(n_chunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(n_chunks)))
     return out.reshape(shape)
 
 

@@ -20,7 +20,10 @@ def _run(*args, timeout=300):
 
 
 def test_reference_arm_json_line():
+    import time
+    t0 = time.time()
     r = _run("--impl", "reference", "--workload", "tiny_fprop", "--steps", "3", "--warmup", "3")
+    wall = time.time() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1, r.stdout
@@ -39,6 +42,17 @@ def test_reference_arm_json_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    # the steps it reports were run, within the process's own wall time
+    assert d["ms_per_step"] * d["steps"] / 1e3 < wall
+    assert d["work_per_step"] > 0
+    assert abs(d["work_per_step"] / (d["ms_per_step"] * 1e-3) / 1e12 - d["value"]) < \
+        0.25 * d["value"]
+    # the same config dict as our arm's line for this workload
+    import bench
+    import numpy as np
+    wl = bench.make_workload("tiny_fprop")
+    assert d["config"] == json.loads(json.dumps(
+        bench.workload_config(wl, wl.in_bytes(wl.host_inputs()), 1)))
 
 
 def test_warmup_below_three_is_rejected():
@@ -96,7 +110,10 @@ def test_our_arm_json_line_on_the_gpu():
               "roofline", "e2e", "gpu_launches", "clocks"):
         assert k in d, k
     assert d["value"] > 0 and d["steps"] == 20 and d["warmup"] == 3
-    assert d["gpu_launches"] == 3 * 20          # quant_act, quant_weight, GEMM per step
+    # quant_act, quant_weight, GEMM per step; the 20-step loop repeated until
+    # the timed region has lasted at least a second
+    assert d["repeats"] >= 1 and d["gpu_launches"] == 3 * 20 * d["repeats"]
+    assert d["timed_s"] >= 0.9
     roof = d["roofline"]
     assert roof["bound"] == "tensor" and roof["kernel"] == "fp8q_gemm_kernel"
     assert roof["peak"] > 0 and abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
@@ -105,3 +122,26 @@ def test_our_arm_json_line_on_the_gpu():
     assert e2e["h2d_bytes_per_step"] == 2 * (256 * 512 + 256 * 512)   # X and W, BF16
     assert e2e["d2h_bytes_per_step"] == 2 * 256 * 256                 # C, BF16
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    assert d["clocks"]["samples"] >= 1, d["clocks"]
+    assert "workloads" not in d                  # only the headline run measures them all
+
+
+@pytest.mark.parametrize("name", [n for _, n in __import__("bench").CONFIG_WORKLOADS] +
+                         ["fprop_4096x7168x7168", "quant_tensor_4096", "quant_weight_16x4096"])
+def test_every_configured_workload_is_known(name):
+    # every workload the headline run measures (and the older names) parses,
+    # and its algorithmic work is positive
+    import bench
+    wl = bench.make_workload(name)
+    assert wl.name == name
+    assert wl.work() > 0
+
+
+def test_quant_weight_names():
+    import bench
+    a = bench.make_workload("quant_weight_7168x7168")
+    assert (a.rows * a.groups, a.cols) == (7168, 7168)
+    b = bench.make_workload("quant_weight_16x4096x7168")
+    assert (b.rows, b.cols, b.groups) == (4096, 7168, 16)
+    c = bench.make_workload("quant_weight_16x4096")
+    assert (c.rows * c.groups, c.cols) == (65536, 7168)
