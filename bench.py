@@ -773,10 +773,11 @@ def make_workload(name: str) -> Workload:
 
 def workload_config(wl: Workload, in_bytes: int, world: int):
     """The line's `config`: the same dict for both arms of one workload."""
+    n = buffer_copies(in_bytes)
     l2 = (f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step > "
-          f"{L2_BYTES / 1e6:.0f} MB); no flush" if in_bytes > L2_BYTES else
-          f"inputs {in_bytes / 1e6:.0f} MB fit in L2: a {2 * L2_BYTES / 1e6:.0f} MB buffer is "
-          "overwritten before every step, outside the kernels' event span")
+          f"{L2_BYTES / 1e6:.0f} MB); no flush" if n == 1 else
+          f"inputs {in_bytes / 1e6:.1f} MB fit in L2: steps cycle through {n} copies of the "
+          f"step's buffers ({n * in_bytes / 1e6:.0f} MB of inputs); no flush")
     return dict(workload=wl.name, **wl.config, l2=l2, parallelism=f"replicas x{world}")
 
 
@@ -822,34 +823,34 @@ def _barrier(world):
 class Timer:
     """The K-step loop of one workload, with CUDA events between its kernels,
     repeated `repeats` times; each repeat sits between a barrier and a device
-    synchronise.  With `flush`, every step first overwrites a buffer larger
-    than L2 (outside the events), so that a workload whose inputs would fit
-    in L2 reads them from HBM; its step time is then the span of its own
-    kernels, first event to last."""
+    synchronise.  `ks_sets` holds one kernel list per copy of the step's
+    buffers; step i runs on copy i % len(ks_sets), so that a workload whose
+    inputs would fit in L2 reads them from HBM (each copy has been evicted by
+    the others by the time it comes round again)."""
 
-    def __init__(self, ks, stream, dev, steps, flush=False):
+    def __init__(self, ks_sets, stream, dev, steps):
         import torch
-        self.ks, self.stream, self.dev, self.steps = ks, stream, dev, steps
-        self.evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ks) + 1)]
+        self.ks_sets, self.stream, self.dev, self.steps = ks_sets, stream, dev, steps
+        self.ks = ks_sets[0]
+        self.i = 0
+        self.evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(self.ks) + 1)]
                     for _ in range(steps)]
         self.e0 = torch.cuda.Event(enable_timing=True)
         self.e1 = torch.cuda.Event(enable_timing=True)
-        self.flush_buf = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-                          if flush else None)
 
     def step(self, ev=None):
-        if self.flush_buf is not None:
-            self.flush_buf.fill_(0x5A)
-        for i, k in enumerate(self.ks):
+        ks = self.ks_sets[self.i % len(self.ks_sets)]
+        self.i += 1
+        for i, k in enumerate(ks):
             if ev is not None:
                 ev[i].record(self.stream)
             k.fn()
         if ev is not None:
-            ev[len(self.ks)].record(self.stream)
+            ev[len(ks)].record(self.stream)
 
     def run(self, repeats, world):
         import torch
-        rep_ms, ksum, spans = [], [0.0] * len(self.ks), []
+        rep_ms, ksum = [], [0.0] * len(self.ks)
         t0 = time.time()
         for _ in range(repeats):
             _barrier(world)
@@ -864,18 +865,31 @@ class Timer:
             for ev in self.evs:
                 for i in range(len(self.ks)):
                     ksum[i] += ev[i].elapsed_time(ev[i + 1])
-                if self.flush_buf is not None:
-                    spans.append(ev[0].elapsed_time(ev[len(self.ks)]))
         t1 = time.time()
         n = repeats * self.steps
-        ms_step = (statistics.median(spans) if spans else statistics.median(rep_ms) / self.steps)
-        return {"ms_step": ms_step, "kernel_ms": [s / n for s in ksum], "t0": t0, "t1": t1,
-                "timed_s": (sum(spans) if spans else sum(rep_ms)) / 1e3}
+        return {"ms_step": statistics.median(rep_ms) / self.steps,
+                "kernel_ms": [s / n for s in ksum], "t0": t0, "t1": t1,
+                "timed_s": sum(rep_ms) / 1e3}
 
 
-def needs_flush(wl, inp):
-    """A step whose inputs fit in L2 gets an L2 flush before it."""
-    return wl.in_bytes(inp) <= L2_BYTES
+MAX_COPIES = 16
+
+
+def buffer_copies(in_bytes):
+    """Copies of the step's buffers to cycle through: enough that the inputs
+    read between two uses of one copy exceed twice the L2 (one copy when the
+    inputs alone are larger than L2)."""
+    if in_bytes > L2_BYTES:
+        return 1
+    return int(min(MAX_COPIES, math.ceil(2 * L2_BYTES / max(in_bytes, 1)) + 1))
+
+
+def kernel_sets(wl, dev, inp, stream, first_st, pin):
+    """The step's kernels on `first_st` and on the extra buffer copies."""
+    sets = [wl.kernels(first_st, stream)]
+    for _ in range(buffer_copies(wl.in_bytes(inp)) - 1):
+        sets.append(wl.kernels(wl.setup(dev, inp, pin=pin), stream))
+    return sets
 
 
 def repeats_for(per_step_s, steps, min_s, world, dev):
@@ -887,20 +901,18 @@ def repeats_for(per_step_s, steps, min_s, world, dev):
 
 
 def warm_up(timer, warmup, dev):
-    """W untimed steps, then one calibration pass of the K-step loop; returns
-    its device time per step (what sizes the repeats of the timed region)."""
+    """W untimed steps (at least one per buffer copy), then one calibration
+    pass of the K-step loop; returns its device time per step (what sizes the
+    repeats of the timed region)."""
     import torch
-    for _ in range(warmup):
+    for _ in range(max(warmup, len(timer.ks_sets))):
         timer.step()
     torch.cuda.synchronize(dev)
     timer.e0.record(timer.stream)
     for i in range(timer.steps):
-        timer.step(timer.evs[i])
+        timer.step()
     timer.e1.record(timer.stream)
     torch.cuda.synchronize(dev)
-    if timer.flush_buf is not None:   # the kernels' span, as the timed region counts it
-        return statistics.median(ev[0].elapsed_time(ev[len(timer.ks)])
-                                 for ev in timer.evs) * 1e-3
     return timer.e0.elapsed_time(timer.e1) * 1e-3 / timer.steps
 
 
@@ -925,8 +937,9 @@ def measure_other(name, dev, stream, args, clk, hbm, fp8_peak):
     wl = make_workload(name)
     inp = wl.host_inputs()
     st = wl.setup(dev, inp, pin=False)
-    ks = wl.kernels(st, stream)
-    timer = Timer(ks, stream, dev, args.steps, flush=needs_flush(wl, inp))
+    sets = kernel_sets(wl, dev, inp, stream, st, False)
+    ks = sets[0]
+    timer = Timer(sets, stream, dev, args.steps)
     per_step = warm_up(timer, args.warmup, dev)
     if B.fp8q_sync_status(stream) != 0:
         raise SystemExit(f"device status error in the warm-up of {name}")
@@ -940,9 +953,10 @@ def measure_other(name, dev, stream, args, clk, hbm, fp8_peak):
            "ms_per_step": round(r["ms_step"], 5), "steps": args.steps, "repeats": reps,
            "timed_s": round(r["timed_s"], 3),
            "config": workload_config(wl, wl.in_bytes(inp), 1),
+           "buffer_copies": len(sets),
            "kernels": kernel_table(ks, r["kernel_ms"], hbm, fp8_peak),
            "clocks": clk.summary(r["t0"], r["t1"])}
-    del st, ks, timer
+    del st, sets, ks, timer
     torch.cuda.empty_cache()
     return res
 
@@ -968,8 +982,9 @@ def run_ours(args, rank, world, local):
     inp = wl.host_inputs()
     st = wl.setup(dev, inp)
     stream = torch.cuda.current_stream(dev)
-    ks = wl.kernels(st, stream)
-    timer = Timer(ks, stream, dev, args.steps, flush=needs_flush(wl, inp))
+    copies = kernel_sets(wl, dev, inp, stream, st, True)
+    ks = copies[0]
+    timer = Timer(copies, stream, dev, args.steps)
 
     per_step = warm_up(timer, args.warmup, dev)
     if B.fp8q_sync_status(stream) != 0:
@@ -1086,6 +1101,7 @@ def run_ours(args, rank, world, local):
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "pipeline": "H2D(i+1) and D2H(i-1) overlap kernels(i); 2 device buffer sets"},
         "gpu_launches": len(ks) * args.steps * reps,
+        "buffer_copies": len(copies),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -1095,7 +1111,7 @@ def run_ours(args, rank, world, local):
         if isinstance(wl, Fprop):
             line["errors"] = gemm_errors(wl, inp, st, ref)
     if world == 1 and args.all_workloads:
-        del st, st2, sets, ks, timer
+        del st, st2, sets, ks, timer, copies
         torch.cuda.empty_cache()
         others = {}
         for _, name in CONFIG_WORKLOADS:

@@ -208,3 +208,32 @@ def test_quant_tensor_workspace_too_small():
     with pytest.raises(B.FP8QError) as e:
         B.fp8q_quant_tensor(x, workspace=ws)
     assert e.value.status == B.FP8Q_ERR_SHAPE
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_scale_of_every_bf16_max_abs(oracle, pow2):
+    # Every positive finite BF16 value (0x0001 .. 0x7F7F) is the max-abs of one
+    # 1x128 group and of one 128x1 channel group: the scales (and the codes of
+    # the group's other values) must equal the oracle's for every possible
+    # max-abs, the subnormal ones going through the 2^-116 floor.
+    vals = np.arange(1, 0x7F80, dtype=np.uint16)
+    M = vals.size
+    x = np.zeros((M, 128), np.uint16)
+    x[:, 0] = vals
+    x[:, 77] = vals | 0x8000            # the same magnitude, negative
+    x[:, 5] = vals >> 1                 # smaller values of the same group
+    q_ref, s_ref = oracle.quant_act(x, pow2)
+    q, s = B.fp8q_quant_act(bf16_to_torch(x), scale_mode=_mode(pow2))
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(q), q_ref, "1x128 codes")
+    assert_scales_equal(f32(s), s_ref, "1x128 scales")
+    C = (M + 7) // 8 * 8                # 128x1: one channel per value
+    xt = np.zeros((128, C), np.uint16)
+    xt[3, :M] = vals
+    xt[100, :M] = vals | 0x8000
+    xt[64, :M] = vals >> 2
+    qT_ref, sT_ref = oracle.quant_act_T(xt, pow2)
+    qT, sT = B.fp8q_quant_act_T(bf16_to_torch(xt), scale_mode=_mode(pow2))
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(qT), qT_ref, "128x1 codes")
+    assert_scales_equal(f32(sT), sT_ref, "128x1 scales")
