@@ -75,7 +75,12 @@ constexpr size_t kRingBytes = static_cast<size_t>(kStages) * (kABytes + kBBytes)
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + kEpiWarps * 32;
 constexpr int kLaunchRegs = 168;                // must match ptxas' count (checked by the build)
+// Register split: the control warpgroup gives registers back, the epilogue
+// warpgroups take them; kernels that prepare per-column scale words in warps
+// 2-3 keep more in the control warpgroup for the loads in flight there.
 constexpr int kCtlRegs = 40, kEpiRegs = 232;
+constexpr int kCtlRegsPrep = 56, kEpiRegsPrep = 224;
+static_assert(kCtlRegsPrep + 2 * kEpiRegsPrep <= 3 * kLaunchRegs, "register split must fit");
 static_assert(kCtlRegs + 2 * kEpiRegs <= 3 * kLaunchRegs, "register split must fit the launch");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kAccBufs * BN;    // accumulators: columns [0, kAccCols)
@@ -115,6 +120,19 @@ struct MxArgs {
   uint64_t timeout_ns;
 };
 
+// Per-column B scale preparation (dense GEMMs with FP8Q_BSCALE_ROW): every
+// scale stage needs 32 FP32 scales per lane (256 columns x 4 K-groups) turned
+// into 8 UE8M0 words per lane.  The two otherwise idle warps of the first
+// warpgroup (warp 2: column groups 0-3, warp 3: 4-7) load and convert them
+// into a shared-memory ring kPrepSlots stages ahead, and the B producer warps,
+// which must write the words into their own TMEM lane quarters and which also
+// drain the accumulator, only copy ready words.  Loaded by the producers
+// themselves, a global load's latency (about a microsecond under the GEMM's
+// own L2 traffic) fell on the critical path each time they caught up after a
+// drain; block scales (8 values per stage) do not need this.
+constexpr int kPrepSlots = 8;
+constexpr size_t kPrepBytes = static_cast<size_t>(kPrepSlots) * 8 * 32 * 4;  // [slot][c][lane]
+
 struct alignas(8) MxCtl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -123,6 +141,8 @@ struct alignas(8) MxCtl {
   uint64_t tfull[kAccBufs];    // every CTA: accumulator complete
   uint64_t tempty[kAccBufs];   // leading CTA: accumulator read (16 warp arrivals)
   uint64_t drain;
+  uint64_t pready[kPrepSlots];  // every CTA: both preparing warps wrote a stage's B words
+  uint64_t pfree[kPrepSlots];   // every CTA: the four B producer warps read them
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -203,13 +223,16 @@ template <int kBScale, bool kOutF32, bool kAccum, bool kGrouped = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8q_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const MxArgs p) {
+  // per-column B scales of a dense GEMM are prepared in warps 2-3
+  constexpr bool kPrep = kBScale == FP8Q_BSCALE_ROW && !kGrouped;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + kStages * kABytes;
   uint8_t *sC = smem + kRingBytes;  // output staging (1024-byte aligned)
-  MxCtl *ctl = reinterpret_cast<MxCtl *>(sC + kStageBytes);
+  uint32_t *prep_b = reinterpret_cast<uint32_t *>(sC + kStageBytes);  // [slot][8][32]
+  MxCtl *ctl = reinterpret_cast<MxCtl *>(sC + kStageBytes + (kPrep ? kPrepBytes : 0));
   int *s_lo = reinterpret_cast<int *>(ctl + 1);  // grouped only (see mx_tile_of)
   int *s_hi = s_lo + (kMaxGroups + 1);
   int *s_pre = s_hi + (kMaxGroups + 1);
@@ -235,6 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->tempty[i]), 2 * kEpiWarps);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
+    for (int i = 0; i < kPrepSlots; ++i) {
+      mbar_init(smem_u32(&ctl->pready[i]), 2);
+      mbar_init(smem_u32(&ctl->pfree[i]), 4);
+    }
     ctl->abort_flag = 0;
     fence_barrier_init();
   }
@@ -277,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp >= 4) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPrep ? kEpiRegsPrep : kEpiRegs));
     // ================================================== scale producers + epilogue
     const int ew = warp - 4;
     const int q = warp & 3;          // lane quarter this warp may access
@@ -307,10 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      : (BN / 128) * kGroupsPerStage;
     // split: a warp loads one side, from raw[0]; combined: A at [0, 4), B after
     constexpr int kOffB = kSplitSides ? 0 : kGroupsPerStage;
-    constexpr int kRaw = kSplitSides ? (kRawB > kGroupsPerStage ? kRawB : kGroupsPerStage)
-                                     : kGroupsPerStage + kRawB;
+    static_assert(!kPrep || kSplitSides, "prepared B words assume split sides");
+    constexpr int kRaw = kPrep ? kGroupsPerStage
+                         : kSplitSides ? (kRawB > kGroupsPerStage ? kRawB : kGroupsPerStage)
+                                       : kGroupsPerStage + kRawB;
     const int NB = (p.N + 127) / 128;
     auto load_raw = [&](int t, int js, float (&r)[kRaw]) {
+      if (kPrep && !do_a) return;  // the B words come from warps 2-3
       const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
       const int kb0 = js * kGroupsPerStage;
 #pragma unroll
@@ -351,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     float raw[kRaw];
+    int gp = 0;                          // stages produced (prepared-word ring position)
     int cur_t = tile_first, cur_js = 0;  // production cursor
     if (cur_t < total_tiles) load_raw(cur_t, 0, raw);
 
@@ -368,6 +399,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float nxt[kRaw];
       if (nt < total_tiles) load_raw(nt, njs, nxt);
+      // prepared words of this stage (warps 2-3), copied to registers and
+      // released before the wait for the TMEM scale slot
+      uint32_t pw[8];
+      if (kPrep && do_b) {
+        const int pslot = gp % kPrepSlots;
+        const bool ready = mbar_wait_bounded(
+            smem_u32(&ctl->pready[pslot]), static_cast<uint32_t>(gp / kPrepSlots) & 1u,
+            abort_flag, &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
+        if (!__all_sync(0xffffffffu, ready)) return false;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) pw[c] = prep_b[(pslot * 8 + c) * 32 + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->pfree[pslot]));
+        ++gp;
+      }
       const bool got = mbar_wait_bounded(smem_u32(&ctl->sempty[ss]), sphase ^ 1, abort_flag,
                                          &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, got)) return false;  // tcgen05.st needs the whole warp
@@ -382,7 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (do_b && !(kSplitSides && do_a)) {
         uint32_t w[8];
-        if (kBScale == FP8Q_BSCALE_ROW) {  // one word per 32-column group
+        if (kPrep) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) w[c] = pw[c];
+        } else if (kBScale == FP8Q_BSCALE_ROW) {  // one word per 32-column group
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t word = 0x7F7F7F7Fu;  // column group past the tile: unused, 2^0
@@ -529,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPrep ? kCtlRegsPrep : kCtlRegs));
   if (warp == 0) {
     // ================================================== TMA producer
     if (lane == 0) {
@@ -566,6 +615,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (armed & (1u << s)) mbar_wait_drain(smem_u32(&ctl->full[s]), (armed_phase >> s) & 1);
         }
         spin_ns(1000000);
+      }
+    }
+  } else if (kPrep && (warp == 2 || warp == 3)) {
+    // ================================================== per-column B scale words
+    // warp 2 prepares column groups 0-3, warp 3 groups 4-7, of scale stage g
+    // (consumption order) into slot g % kPrepSlots
+    const int c0 = (warp - 2) * 4;
+    int g = 0;
+    bool ok = true;
+    for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
+      const MxTile tl = mx_tile_of<kGrouped>(t, p, s_lo, s_hi, s_pre);
+      for (int js = 0; js < nst; ++js, ++g) {
+        const int kb0 = js * kGroupsPerStage;
+        const int slot = g % kPrepSlots;
+        // loads first: their latency overlaps the wait for the slot
+        float v[4 * kGroupsPerStage];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int n = tl.n0 + 32 * (c0 + c) + lane;
+#pragma unroll
+          for (int j = 0; j < kGroupsPerStage; ++j)
+            v[4 * c + j] = kb0 + j < p.num_kb && n < p.N
+                               ? __ldg(p.sb + static_cast<int64_t>(kb0 + j) * p.ld_sb + n)
+                               : 1.0f;
+        }
+        const bool got = mbar_wait_bounded(
+            smem_u32(&ctl->pfree[slot]), (static_cast<uint32_t>(g / kPrepSlots) & 1u) ^ 1u,
+            abort_flag, &g_mx_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        bool bad = false;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int j = 0; j < kGroupsPerStage; ++j) w |= ue8m0_of(v[4 * c + j], bad) << (8 * j);
+          prep_b[(slot * 8 + c0 + c) * 32 + lane] = c0 + c < kBCols32 ? w : 0x7F7F7F7Fu;
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(&g_mx_status, 0, FP8Q_ERR_INVALID);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->pready[slot]));
       }
     }
   } else if (warp == 1) {
@@ -649,7 +741,9 @@ template <int kBScale, bool kOutF32, bool kAccum, bool kGrouped = false>
 fp8q_status launch_mx(const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs &args,
                       int64_t tiles, cudaStream_t s) {
   auto kern = fp8q_gemm_mx_kernel<kBScale, kOutF32, kAccum, kGrouped>;
-  constexpr size_t smem = kSmemBytes + (kGrouped ? kGroupTables : 0);
+  constexpr size_t smem = kSmemBytes + (kGrouped ? kGroupTables : 0) +
+                          (kBScale == FP8Q_BSCALE_ROW && !kGrouped ? kPrepBytes : 0);
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
   static int max_pairs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
@@ -738,7 +832,7 @@ fp8q_status mx_entry(const void *a, int64_t lda, const float *sa, int64_t ld_sa,
   if (bkind == FP8Q_BSCALE_BLOCK && ld_sb < KB) return FP8Q_ERR_SHAPE;
   if (bkind == FP8Q_BSCALE_BLOCK_T && ld_sb < NB) return FP8Q_ERR_SHAPE;
   if (bkind == FP8Q_BSCALE_ROW && ld_sb < N) return FP8Q_ERR_SHAPE;
-  if (dev.max_smem_optin < static_cast<int>(kSmemBytes)) return FP8Q_ERR_UNSUPPORTED;
+  if (dev.max_smem_optin < static_cast<int>(kSmemBytes + kPrepBytes)) return FP8Q_ERR_UNSUPPORTED;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K, lda, 128, BM,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
