@@ -491,7 +491,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int wrow0 = tl.m0 + row_in_tile - lane;
       const bool warp_ok = wrow0 < tl.row_end && ncol0 < p.N;  // warp-uniform
       const uint32_t buf = smem_u32(sC) + static_cast<uint32_t>(ew) * 2048u;
-      if (kOutF32) {
+      if (kOutF32 && kPrep) {
+        // FP32 out, per-column scales: these warps hold no raw scales, so the
+        // whole row of kEpiCols values is read first and the accumulator is
+        // released before any store; stores go 64 bytes (16 columns) of each
+        // row at a time through the warp's buffer
+        uint32_t v[kChunks][16];
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) tmem_ld_32x32b_x16(taddr + i * 16, v[i]);
+        tmem_wait_ld_tied(v[0]);
+#pragma unroll
+        for (int i = 1; i < kChunks; ++i) reg_tie(v[i]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(buf_acc) * 8u);
+        if (warp_ok) {
+#pragma unroll
+          for (int i = 0; i < kChunks; ++i) {
+            const int col = ncol0 + i * 16;
+            if (col >= p.N) break;
+            uint4 u[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              u[q] = make_uint4(v[i][4 * q], v[i][4 * q + 1], v[i][4 * q + 2], v[i][4 * q + 3]);
+            warp_store_block64<4, kAccum>(buf, u, p.c, p.ldc, wrow0, tl.row_end, col, p.N, lane);
+          }
+        }
+      } else if (kOutF32) {
         // FP32 out: two halves of kEpiCols / 2 columns, the first stored while
         // the second is read, which halves the registers the drain holds; the
         // accumulator is released after the last TMEM read.  Stores go 64
