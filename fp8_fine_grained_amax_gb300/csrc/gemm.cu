@@ -314,35 +314,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = tile_first; ok && t < total_tiles; t += tile_step) {
       const Tile tl = tile_of<kGrouped, C::kTileM>(t, p, s_lo, s_prefix);
       const int m = tl.a_row + row_in_tile;
-      const bool row_in = m < p.M;
       const int ncol0 = tl.n0 + col_base;
       const int nb = ncol0 / 128;
       const float *sb_g = p.sb;
       if (kGrouped) sb_g += static_cast<int64_t>(tl.g) * NB * p.num_kb;
-      // scales of K-group kb: sa of this row; sb of this warp's columns
-      // (block kinds: one value; per-column kind: lane l holds the 4 scales
-      // of columns 4l..4l+3 of the warp's kEpiCols, staged in shared memory)
-      auto load_sa = [&](int kb) {
-        return row_in ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ld_sa + m) : 0.0f;
+      // Scales of K-group kb: sa of this row; sb of this warp's columns (block
+      // kinds: one value; per-column kind: lane l holds the 4 scales of
+      // columns 4l..4l+3 of the warp's kEpiCols, staged in shared memory).
+      // Pointers to group 0's values advance by one group's stride per group;
+      // rows past M, blocks past N and columns past N read as 0.
+      const bool sa_in = m < p.M;
+      const float *sa_ptr = p.sa + (sa_in ? m : 0);
+      const bool sb_in = kBScale == FP8Q_BSCALE_ROW || nb < NB;
+      const float *sb_ptr =
+          kBScale == FP8Q_BSCALE_BLOCK
+              ? sb_g + static_cast<int64_t>(sb_in ? nb : 0) * (kGrouped ? p.num_kb : p.ld_sb)
+          : kBScale == FP8Q_BSCALE_BLOCK_T ? p.sb + (sb_in ? nb : 0)
+                                           : p.sb + ncol0 + 4 * lane;
+      const int64_t sb_step = kBScale == FP8Q_BSCALE_BLOCK ? 1 : p.ld_sb;
+      const int ncol = ncol0 + 4 * lane;  // per-column kind: this lane's first column
+      auto load_sa = [&]() { return sa_in ? __ldg(sa_ptr) : 0.0f; };
+      auto load_sb = [&]() {
+        return kBScale != FP8Q_BSCALE_ROW && sb_in ? __ldg(sb_ptr) : 0.0f;
       };
-      auto load_sb = [&](int kb) {
-        if (kBScale == FP8Q_BSCALE_BLOCK)
-          return nb < NB ? __ldg(sb_g + static_cast<int64_t>(nb) * (kGrouped ? p.num_kb : p.ld_sb) +
-                                 kb)
-                         : 0.0f;
-        if (kBScale == FP8Q_BSCALE_BLOCK_T)
-          return nb < NB ? __ldg(p.sb + static_cast<int64_t>(kb) * p.ld_sb + nb) : 0.0f;
-        return 0.0f;
-      };
-      auto load_sb4 = [&](int kb) {
+      auto load_sb4 = [&]() {
         float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (kBScale == FP8Q_BSCALE_ROW) {
-          const int n = ncol0 + 4 * lane;
-          const float *src = p.sb + static_cast<int64_t>(kb) * p.ld_sb + n;
-          if (n + 0 < p.N) v.x = __ldg(src + 0);
-          if (n + 1 < p.N) v.y = __ldg(src + 1);
-          if (n + 2 < p.N) v.z = __ldg(src + 2);
-          if (n + 3 < p.N) v.w = __ldg(src + 3);
+          if (ncol + 0 < p.N) v.x = __ldg(sb_ptr + 0);
+          if (ncol + 1 < p.N) v.y = __ldg(sb_ptr + 1);
+          if (ncol + 2 < p.N) v.z = __ldg(sb_ptr + 2);
+          if (ncol + 3 < p.N) v.w = __ldg(sb_ptr + 3);
         }
         return v;
       };
@@ -350,18 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t acc[kEpiCols / 2];  // packed FP32 pairs: columns (2i, 2i+1) of this thread's
 #pragma unroll
       for (int j = 0; j < kEpiCols / 2; ++j) acc[j] = 0ull;
-      float sa_nx = p.num_kb > 0 ? load_sa(0) : 0.0f;
-      float sb_nx = p.num_kb > 0 ? load_sb(0) : 0.0f;
-      float4 sb4_nx = p.num_kb > 0 ? load_sb4(0) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float sa_nx = p.num_kb > 0 ? load_sa() : 0.0f;
+      float sb_nx = p.num_kb > 0 ? load_sb() : 0.0f;
+      float4 sb4_nx = p.num_kb > 0 ? load_sb4() : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 
       for (int kb = 0; kb < p.num_kb; ++kb) {
         // the scales of group kb were loaded one iteration ago; fetch kb+1 now
         const float sa_v = sa_nx, sb_v = sb_nx;
         const float4 sb4 = sb4_nx;
         if (kb + 1 < p.num_kb) {
-          sa_nx = load_sa(kb + 1);
-          sb_nx = load_sb(kb + 1);
-          sb4_nx = load_sb4(kb + 1);
+          sa_ptr += p.ld_sa;
+          sb_ptr += sb_step;
+          sa_nx = load_sa();
+          sb_nx = load_sb();
+          sb4_nx = load_sb4();
         }
         if (kBScale == FP8Q_BSCALE_ROW) {
           // the buffer written here was last read two K-groups ago, before the
