@@ -28,7 +28,11 @@ Prints ONE JSON line (rank 0).  `value` is the step's algorithmic work (GEMM
 FLOPs 2MNK over real rows, or quantiser bytes) summed over ranks per second of
 device time.  The timed region is the K-step loop, repeated until it has run
 for at least --min-seconds (each repeat between a barrier and a device
-synchronise); the median repeat gives `ms_per_step`.  The per-kernel times, the
+synchronise); the median repeat gives `ms_per_step`.  The K-step loop is
+captured once as a CUDA graph and replayed (--no-graph launches it from the
+host instead), so that the device runs the kernels back to back rather than
+waiting on host launch overhead; the per-kernel times come from timing events
+between the kernels inside the graph.  The per-kernel times, the
 roofline of the dominant kernel, an end-to-end number through host buffers,
 the clocks sampled during the timed region, the error of the result against
 the CPU oracle, the CPU oracle's own throughput, and (one GPU) the same
@@ -820,27 +824,51 @@ def _barrier(world):
         dist.barrier()
 
 
+def _graph_events_supported():
+    """CUDA events that a graph capture records as timing nodes (torch's
+    `external` events) exist in this torch."""
+    import inspect
+
+    import torch
+    try:
+        return "external" in inspect.signature(torch.cuda.Event.__new__).parameters
+    except (TypeError, ValueError):
+        return False
+
+
 class Timer:
     """The K-step loop of one workload, with CUDA events between its kernels,
     repeated `repeats` times; each repeat sits between a barrier and a device
     synchronise.  `ks_sets` holds one kernel list per copy of the step's
     buffers; step i runs on copy i % len(ks_sets), so that a workload whose
     inputs would fit in L2 reads them from HBM (each copy has been evicted by
-    the others by the time it comes round again)."""
+    the others by the time it comes round again).
 
-    def __init__(self, ks_sets, stream, dev, steps):
+    With `graph`, the K-step loop is captured once as a CUDA graph (one graph
+    per starting copy, so that copies keep rotating across repeats) and each
+    repeat replays it: the device runs the kernels back to back instead of
+    waiting for the host to launch each one, and the events between the
+    kernels are timing nodes of the graph."""
+
+    def __init__(self, ks_sets, stream, dev, steps, graph=True):
         import torch
         self.ks_sets, self.stream, self.dev, self.steps = ks_sets, stream, dev, steps
         self.ks = ks_sets[0]
         self.i = 0
-        self.evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(self.ks) + 1)]
+        self.graph = bool(graph) and _graph_events_supported()
+        kw = {"external": True} if self.graph else {}
+        self.evs = [[torch.cuda.Event(enable_timing=True, **kw) for _ in range(len(self.ks) + 1)]
                     for _ in range(steps)]
         self.e0 = torch.cuda.Event(enable_timing=True)
         self.e1 = torch.cuda.Event(enable_timing=True)
+        self.graphs = []
+        self.graph_error = None
 
-    def step(self, ev=None):
-        ks = self.ks_sets[self.i % len(self.ks_sets)]
-        self.i += 1
+    def step(self, ev=None, at=None):
+        if at is None:
+            at = self.i
+            self.i += 1
+        ks = self.ks_sets[at % len(self.ks_sets)]
         for i, k in enumerate(ks):
             if ev is not None:
                 ev[i].record(self.stream)
@@ -848,16 +876,54 @@ class Timer:
         if ev is not None:
             ev[len(ks)].record(self.stream)
 
+    def capture(self):
+        """Capture the timed loop (after eager warm-up steps have run every
+        kernel once).  Falls back to eager launches if capture fails."""
+        import torch
+        if not self.graph:
+            return
+        c = len(self.ks_sets)
+        try:
+            for j in range(c // math.gcd(self.steps, c)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream, capture_error_mode="thread_local"):
+                    for i in range(self.steps):
+                        self.step(self.evs[i], at=j * self.steps + i)
+                self.graphs.append(g)
+        except RuntimeError as e:  # keep the eager loop
+            self.graph_error = str(e).splitlines()[0][:200]
+            self.graphs = []
+            self.graph = False
+            torch.cuda.synchronize(self.dev)
+
+    def loop(self, r):
+        """Repeat r of the K-step loop (graph replay or eager launches)."""
+        import torch
+        if self.graphs:
+            with torch.cuda.stream(self.stream):
+                self.graphs[r % len(self.graphs)].replay()
+        else:
+            for i in range(self.steps):
+                self.step(self.evs[i])
+
+    def mode(self):
+        if self.graphs:
+            return {"mode": "cuda_graph", "graphs": len(self.graphs),
+                    "kernel_events": "timing nodes between the kernels of the graph"}
+        out = {"mode": "eager", "kernel_events": "events recorded between launches"}
+        if self.graph_error:
+            out["graph_error"] = self.graph_error
+        return out
+
     def run(self, repeats, world):
         import torch
         rep_ms, ksum = [], [0.0] * len(self.ks)
         t0 = time.time()
-        for _ in range(repeats):
+        for r in range(repeats):
             _barrier(world)
             torch.cuda.synchronize(self.dev)
             self.e0.record(self.stream)
-            for i in range(self.steps):
-                self.step(self.evs[i])
+            self.loop(r)
             self.e1.record(self.stream)
             torch.cuda.synchronize(self.dev)
             _barrier(world)
@@ -901,16 +967,16 @@ def repeats_for(per_step_s, steps, min_s, world, dev):
 
 
 def warm_up(timer, warmup, dev):
-    """W untimed steps (at least one per buffer copy), then one calibration
-    pass of the K-step loop; returns its device time per step (what sizes the
-    repeats of the timed region)."""
+    """W untimed steps (at least one per buffer copy), the capture of the
+    timed loop, then one calibration pass of it; returns its device time per
+    step (what sizes the repeats of the timed region)."""
     import torch
     for _ in range(max(warmup, len(timer.ks_sets))):
         timer.step()
     torch.cuda.synchronize(dev)
+    timer.capture()
     timer.e0.record(timer.stream)
-    for i in range(timer.steps):
-        timer.step()
+    timer.loop(0)
     timer.e1.record(timer.stream)
     torch.cuda.synchronize(dev)
     return timer.e0.elapsed_time(timer.e1) * 1e-3 / timer.steps
@@ -939,7 +1005,7 @@ def measure_other(name, dev, stream, args, clk, hbm, fp8_peak):
     st = wl.setup(dev, inp, pin=False)
     sets = kernel_sets(wl, dev, inp, stream, st, False)
     ks = sets[0]
-    timer = Timer(sets, stream, dev, args.steps)
+    timer = Timer(sets, stream, dev, args.steps, graph=args.graph)
     per_step = warm_up(timer, args.warmup, dev)
     if B.fp8q_sync_status(stream) != 0:
         raise SystemExit(f"device status error in the warm-up of {name}")
@@ -954,6 +1020,7 @@ def measure_other(name, dev, stream, args, clk, hbm, fp8_peak):
            "timed_s": round(r["timed_s"], 3),
            "config": workload_config(wl, wl.in_bytes(inp), 1),
            "buffer_copies": len(sets),
+           "timing": timer.mode(),
            "kernels": kernel_table(ks, r["kernel_ms"], hbm, fp8_peak),
            "clocks": clk.summary(r["t0"], r["t1"])}
     del st, sets, ks, timer
@@ -981,10 +1048,12 @@ def run_ours(args, rank, world, local):
     wl = make_workload(args.workload)
     inp = wl.host_inputs()
     st = wl.setup(dev, inp)
-    stream = torch.cuda.current_stream(dev)
+    # a stream of its own: the legacy default stream cannot be captured
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
     copies = kernel_sets(wl, dev, inp, stream, st, True)
     ks = copies[0]
-    timer = Timer(copies, stream, dev, args.steps)
+    timer = Timer(copies, stream, dev, args.steps, graph=args.graph)
 
     per_step = warm_up(timer, args.warmup, dev)
     if B.fp8q_sync_status(stream) != 0:
@@ -1094,6 +1163,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic",
         "config": workload_config(wl, wl.in_bytes(inp), world),
         "roofline": roof,
+        "timing": timer.mode(),
         "kernels": dict(kernels, hbm_peak_gbs=hbm, fp8_peak_tflops=round(fp8_peak, 1),
                         peak_source=src),
         "e2e": {"value": round(whole_job_value(work, world, e2e_ms, scale), 2), "unit": wl.unit,
@@ -1172,6 +1242,8 @@ def main():
                     help="shortest timed region per workload (repeats of the K-step loop)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false", default=True,
+                    help="launch the timed loop eagerly instead of replaying it as a CUDA graph")
     ap.add_argument("--all-workloads", dest="all_workloads", action="store_true", default=None,
                     help="also measure every other configuration's workloads (default: on for "
                          "the headline workload on one GPU)")
