@@ -302,9 +302,18 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 // ring); they are decoded exactly (E4M3 is a subset of FP16) into a
 // 128-byte-swizzled FP16 tile; ldmatrix.trans reads it by channel; the
 // transposed codes leave through one TMA store.  The next tile's row scales
-// are loaded while this one is processed.
+// are loaded while this one is processed.  Tiles are 128 tokens x 64 channels
+// (a 64-channel tile lies inside one 128-channel group of the row scales), so
+// that a CTA needs 48 KB of shared memory and four CTAs share an SM: the
+// decode, reduce and store phases of a tile are separated by CTA barriers,
+// and other CTAs' phases fill the gaps.  Warp w of 8 owns channels 8w..8w+7.
+constexpr int kRqCh = 64;                                  // channels per tile
+constexpr int kRqThreads = 256;
+constexpr uint32_t kRqRawBytes = 128 * kRqCh;              // raw codes, 64-byte rows
+constexpr uint32_t kRqF16Bytes = 128 * kRqCh * 2;          // FP16 tile, 128-byte rows
+constexpr uint32_t kRqStageBytes = kRqCh * 128;            // transposed codes
 template <bool kPow2>
-__global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
+__global__ void __launch_bounds__(kRqThreads, 4) requant_act_T_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQT, int64_t T,
     int64_t C, const float *__restrict__ s_rows, int64_t ld_s_rows, float *__restrict__ sT,
     int64_t ld_sT, uint64_t timeout_ns) {
@@ -312,22 +321,22 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
   __shared__ __align__(16) float srow[128];
   __shared__ uint64_t full[2];
   __shared__ int abort_flag;
-  const uint32_t raw0 = (smem_u32(dsm_raw) + 1023u) & ~1023u;  // 2 x 16 KB raw codes
-  const uint32_t tin = raw0 + 2 * kTileBytesQ;                // 2 x 16 KB FP16 halves
-  const uint32_t st0 = tin + kTileBytesBF16;                   // 2 x 16 KB staged codes
+  const uint32_t raw0 = (smem_u32(dsm_raw) + 1023u) & ~1023u;  // 2 x 8 KB raw codes
+  const uint32_t tin = raw0 + 2 * kRqRawBytes;                // 16 KB FP16 tile
+  const uint32_t st0 = tin + kRqF16Bytes;                      // 2 x 8 KB staged codes
 
-  const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
-  const int64_t ncb = C / 128;
+  const int tid = threadIdx.x, hw = tid >> 3, l8 = tid & 7;
+  const int64_t ncb = C / kRqCh;
   const int64_t ntiles = ncb * (T / 128);
   int pending[2] = {-1, -1};
   auto issue_load = [&](int b, int64_t t) {
     const uint32_t bar = smem_u32(&full[b]);
-    mbar_arrive_expect_tx(bar, kTileBytesQ);
-    tma_load_2d(raw0 + b * kTileBytesQ, &tmQ, bar, static_cast<int32_t>((t % ncb) * 128),
+    mbar_arrive_expect_tx(bar, kRqRawBytes);
+    tma_load_2d(raw0 + b * kRqRawBytes, &tmQ, bar, static_cast<int32_t>((t % ncb) * kRqCh),
                 static_cast<int32_t>((t / ncb) * 128));
   };
   auto row_scale = [&](int64_t t) {  // threads < 128: this tile's scale of token row tid
-    return s_rows[(t % ncb) * ld_s_rows + (t / ncb) * 128 + tid];
+    return s_rows[((t % ncb) * kRqCh / 128) * ld_s_rows + (t / ncb) * 128 + tid];
   };
   if (tid == 0) {
     mbar_init(smem_u32(&full[0]), 1);
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
   __syncthreads();
 
   const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t h = static_cast<uint32_t>(warp >> 3), j = static_cast<uint32_t>(warp & 7);
+  const uint32_t j = static_cast<uint32_t>(warp);  // the warp's 16-byte chunk of each FP16 row
   const int cw = 8 * warp + (lane >> 2);  // this thread's channel within the tile
   int it = 0;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
@@ -363,21 +372,21 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
       return;
     }
     if (tid == 0) pending[buf] = -1;
-    const int64_t c0 = (t % ncb) * 128, t0 = (t / ncb) * 128;
+    const int64_t c0 = (t % ncb) * kRqCh, t0 = (t / ncb) * 128;
     if (tid < 128) {
       srow[tid] = sr_next;
       if (t + gridDim.x < ntiles) sr_next = row_scale(t + gridDim.x);
     }
-    // decode: thread (hw, l16) takes 8 codes of token rows hw + 32 i
+    // decode: thread (hw, l8) takes 8 codes of token rows hw + 32 i
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t r = static_cast<uint32_t>(hw + 32 * i);
       uint2 q8;
       asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                    : "=r"(q8.x), "=r"(q8.y)
-                   : "r"(raw0 + buf * kTileBytesQ + r * 128u + 8u * l16));
+                   : "r"(raw0 + buf * kRqRawBytes + r * static_cast<uint32_t>(kRqCh) + 8u * l8));
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                       tin + (l16 >> 3) * kHalfBytesBF16 + swz128(r, static_cast<uint32_t>(l16 & 7))),
+                       tin + swz128(r, static_cast<uint32_t>(l8))),
                    "r"(decode_e4m3x2(static_cast<uint16_t>(q8.x & 0xFFFF))),
                    "r"(decode_e4m3x2(static_cast<uint16_t>(q8.x >> 16))),
                    "r"(decode_e4m3x2(static_cast<uint16_t>(q8.y & 0xFFFF))),
@@ -399,7 +408,7 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
       uint32_t r4[4];
-      ldmatrix_x4_trans(tin + h * kHalfBytesBF16 + swz128(32u * qd + lane, j), r4);
+      ldmatrix_x4_trans(tin + swz128(32u * qd + lane, j), r4);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int m = 4 * qd + e;
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(kTileThreads) requant_act_T_kernel(
 
     if (tid == 0) bulk_wait_group_read<1>();  // stage `buf`: its store two tiles ago has read it
     __syncthreads();  // every thread is done with the FP16 tile and row scales
-    const uint32_t stg = st0 + buf * kTileBytesQ;
+    const uint32_t stg = st0 + buf * kRqStageBytes;
 #pragma unroll
     for (int m = 0; m < 16; ++m)
       st_shared_u16(stg + swz128(static_cast<uint32_t>(cw), static_cast<uint32_t>(m >> 1)) +
@@ -654,8 +663,8 @@ fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX,
                    q_rows, ldq_rows, s_rows, ld_s_rows, timeout_ns);
 }
 
-constexpr size_t kRequantSmem = 2 * kTileBytesQ + kTileBytesBF16 + 2 * kTileBytesQ + 1024;
-constexpr int kRequantCtasPerSm = 2;
+constexpr size_t kRequantSmem = 2 * kRqRawBytes + kRqF16Bytes + 2 * kRqStageBytes + 1024;
+constexpr int kRequantCtasPerSm = 4;
 
 template <bool kPow2>
 fp8q_status launch_requant(unsigned grid, cudaStream_t s, const CUtensorMap &tmQ,
@@ -675,7 +684,7 @@ fp8q_status launch_requant(unsigned grid, cudaStream_t s, const CUtensorMap &tmQ
       attr_set[dev] = true;
     }
   }
-  return launch_on(kern, dim3(grid), dim3(kTileThreads), kRequantSmem, s, tmQ, tmQT, T, C, s_rows,
+  return launch_on(kern, dim3(grid), dim3(kRqThreads), kRequantSmem, s, tmQ, tmQT, T, C, s_rows,
                    ld_s_rows, sT, ld_sT, timeout_ns);
 }
 
@@ -844,15 +853,17 @@ extern "C" fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, i
     return FP8Q_ERR_ALIGN;
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  CUtensorMap tmQ, tmQT;  // codes [T][C] and qT [C][T], 128 x 128-byte boxes
+  // codes [T][C] in boxes of 128 tokens x 64 bytes; qT [C][T] in boxes of 64
+  // channel rows x 128 bytes
+  CUtensorMap tmQ, tmQT;
   if (!make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, static_cast<uint64_t>(T),
-                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldq), 128, 128,
+                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldq), kRqCh, 128,
                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_tmap_2d(&tmQT, CU_TENSOR_MAP_DATA_TYPE_UINT8, qT, static_cast<uint64_t>(C),
-                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, 128,
+                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, kRqCh,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return FP8Q_ERR_CUDA;
-  const int64_t ntiles = (C / 128) * (T / 128);
+  const int64_t ntiles = (C / kRqCh) * (T / 128);
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * kRequantCtasPerSm;
   const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
   auto s = static_cast<cudaStream_t>(stream);
