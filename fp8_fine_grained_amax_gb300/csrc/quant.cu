@@ -65,13 +65,20 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   return v;
 }
 
+// Two BF16 values (one 32-bit word) times inv -> two E4M3 codes: one packed
+// FP32 multiply (mul.rn.f32x2 rounds each lane as __fmul_rn does and keeps
+// subnormals) and one convert.
+__device__ __forceinline__ uint32_t quantise2(uint32_t w, uint64_t inv2) {
+  const float2 p = unpack_f32x2(fmul2(pack_f32x2(bf16_lo(w), bf16_hi(w)), inv2));
+  return pack_e4m3x2(p.x, p.y);
+}
+
 // 8 BF16 values times inv -> 8 E4M3 codes (little-endian order kept).
 __device__ __forceinline__ uint2 quantise8(const uint4 &v, float inv) {
+  const uint64_t inv2 = pack_f32x2(inv, inv);
   uint2 r;
-  r.x = pack_e4m3x4(__fmul_rn(bf16_lo(v.x), inv), __fmul_rn(bf16_hi(v.x), inv),
-                    __fmul_rn(bf16_lo(v.y), inv), __fmul_rn(bf16_hi(v.y), inv));
-  r.y = pack_e4m3x4(__fmul_rn(bf16_lo(v.z), inv), __fmul_rn(bf16_hi(v.z), inv),
-                    __fmul_rn(bf16_lo(v.w), inv), __fmul_rn(bf16_hi(v.w), inv));
+  r.x = quantise2(v.x, inv2) | (quantise2(v.y, inv2) << 16);
+  r.y = quantise2(v.z, inv2) | (quantise2(v.w, inv2) << 16);
   return r;
 }
 
@@ -225,21 +232,29 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
     const int64_t c0 = (t % ncb) * 128, t0 = (t / ncb) * 128;
 
     if (kRows) {  // C % 128 == 0 here: every chunk is in range
-      const int hw = tid >> 4, l16 = tid & 15;
+      // eight lanes per token row, 16 channels (two 16-byte chunks) each
+      const int tr = tid >> 3, l8 = tid & 7;
+      const uint32_t half = static_cast<uint32_t>(l8 >> 2) * kHalfBytesBF16;
+      const uint32_t ch0 = static_cast<uint32_t>(2 * l8) & 7u;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t r = static_cast<uint32_t>(hw + 32 * i);
-        uint4 v;
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t r = static_cast<uint32_t>(tr + 64 * i);
+        uint4 v0, v1;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "r"(tin + (l16 >> 3) * kHalfBytesBF16 + swz128(r, l16 & 7)));
-        uint32_t mb = absmax_bits8(v);
+                     : "=r"(v0.x), "=r"(v0.y), "=r"(v0.z), "=r"(v0.w)
+                     : "r"(tin + half + swz128(r, ch0)));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v1.x), "=r"(v1.y), "=r"(v1.z), "=r"(v1.w)
+                     : "r"(tin + half + swz128(r, ch0 + 1)));
+        uint32_t mb = umax16x2(absmax_bits8(v0), absmax_bits8(v1));
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+        for (int o = 4; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
         float sc, inv;
         group_scale(bits_to_f32_max(mb), kPow2, sc, inv);
-        *reinterpret_cast<uint2 *>(q_rows + (t0 + r) * ldq_rows + c0 + l16 * 8) = quantise8(v, inv);
-        if (l16 == 0) s_rows[(c0 / 128) * ld_s_rows + t0 + r] = sc;
+        const uint2 lo = quantise8(v0, inv), hi = quantise8(v1, inv);
+        *reinterpret_cast<uint4 *>(q_rows + (t0 + r) * ldq_rows + c0 + l8 * 16) =
+            make_uint4(lo.x, lo.y, hi.x, hi.y);
+        if (l8 == 0) s_rows[(c0 / 128) * ld_s_rows + t0 + r] = sc;
       }
     }
 
@@ -261,9 +276,9 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
     group_scale(bits_to_f32_max(mw), kPow2, sc, inv);
     if ((lane & 3) == 0 && c0 + cw < C) sT[(t0 / 128) * ld_sT + c0 + cw] = sc;
     uint32_t code[16];  // tokens 8m + 2(lane%4), +1 of channel cw
+    const uint64_t inv2 = pack_f32x2(inv, inv);
 #pragma unroll
-    for (int m = 0; m < 16; ++m)
-      code[m] = pack_e4m3x2(__fmul_rn(bf16_lo(v[m]), inv), __fmul_rn(bf16_hi(v[m]), inv));
+    for (int m = 0; m < 16; ++m) code[m] = quantise2(v[m], inv2);
 
     // the staged codes written two tiles ago must have been read by their store
     if (tid == 0) bulk_wait_group_read<1>();
