@@ -100,6 +100,48 @@ __device__ __forceinline__ float bits_to_f32_max(uint32_t packed) {
   return __uint_as_float((hi > lo ? hi : lo) << 16);
 }
 
+// FP32-mode scales of BF16 max-abs values from two 128-entry tables.  After
+// the 2^-116 floor a BF16 max-abs is a = (1 + m/128) * 2^E with E >= -116,
+// and a / 448 = fl(M / 448) * 2^E, 448 / a = fl(448 / M) * 2^-E exactly, M =
+// 1 + m/128: scaling by a power of two commutes with rounding while the
+// result stays normal, and s and inv stay within [2^-125, 2^125].  The
+// tables hold the IEEE quotients (__fdiv_rn) of the 128 mantissas; an
+// infinite or NaN max-abs goes through group_scale() itself.
+struct ScaleTables {
+  uint32_t s[128];    // bits of fl(M / 448)
+  uint32_t inv[128];  // bits of fl(448 / M)
+};
+
+// Threads 0..127 fill entry tid; the caller synchronises before use.
+__device__ __forceinline__ void scale_tables_init(ScaleTables &t, int tid) {
+  if (tid < 128) {
+    const float M = 1.0f + static_cast<float>(tid) * 0x1p-7f;
+    t.s[tid] = __float_as_uint(__fdiv_rn(M, 448.0f));
+    t.inv[tid] = __float_as_uint(__fdiv_rn(448.0f, M));
+  }
+}
+
+// Scale of a group from the packed 16-bit max-abs patterns of two BF16 lanes
+// (as umax16x2 leaves them): equal to group_scale(bits_to_f32_max(packed)).
+__device__ __forceinline__ void group_scale_bf16(const ScaleTables &t, uint32_t packed, bool pow2,
+                                                 float &s, float &inv) {
+  if (pow2) {
+    group_scale(bits_to_f32_max(packed), true, s, inv);
+    return;
+  }
+  const uint32_t hi = packed >> 16, lo = packed & 0xFFFFu;
+  uint32_t b = (hi > lo ? hi : lo) << 16;  // FP32 bits of the max-abs
+  if (b < 0x05800000u) b = 0x05800000u;    // 2^-116
+  if (b >= 0x7F800000u) {
+    group_scale(__uint_as_float(b), false, s, inv);
+    return;
+  }
+  const uint32_t m = (b >> 16) & 0x7Fu;
+  const uint32_t e = (b >> 23) - 127u;  // E mod 2^32: added to the exponent field
+  s = __uint_as_float(t.s[m] + (e << 23));
+  inv = __uint_as_float(t.inv[m] - (e << 23));
+}
+
 // ------------------------------------------------------------------ 1x128
 // Grid (ceil(M / 64), K / 128).  A CTA handles 64 rows of one 128-wide column
 // group.  Eight lanes own one row's group (16 BF16 = 32 bytes each), so a
@@ -184,8 +226,10 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
   const uint32_t st0 = in0 + 2 * kTileBytesBF16;          // 2 x 16 KB staged codes
   __shared__ uint64_t full[2];
   __shared__ int abort_flag;
+  __shared__ ScaleTables tabs;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  scale_tables_init(tabs, tid);  // visible after the __syncthreads below
   const int64_t ncb = (C + 127) / 128;
   const int64_t ntiles = ncb * (T / 128);
   int pending[2] = {-1, -1};  // thread 0: parity of the copy in flight per buffer
@@ -250,7 +294,7 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 #pragma unroll
         for (int o = 4; o > 0; o >>= 1) mb = umax16x2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
         float sc, inv;
-        group_scale(bits_to_f32_max(mb), kPow2, sc, inv);
+        group_scale_bf16(tabs, mb, kPow2, sc, inv);
         const uint2 lo = quantise8(v0, inv), hi = quantise8(v1, inv);
         *reinterpret_cast<uint4 *>(q_rows + (t0 + r) * ldq_rows + c0 + l8 * 16) =
             make_uint4(lo.x, lo.y, hi.x, hi.y);
@@ -273,7 +317,7 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
     mw = umax16x2(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
     mw = umax16x2(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
     float sc, inv;
-    group_scale(bits_to_f32_max(mw), kPow2, sc, inv);
+    group_scale_bf16(tabs, mw, kPow2, sc, inv);
     if ((lane & 3) == 0 && c0 + cw < C) sT[(t0 / 128) * ld_sT + c0 + cw] = sc;
     uint32_t code[16];  // tokens 8m + 2(lane%4), +1 of channel cw
     const uint64_t inv2 = pack_f32x2(inv, inv);

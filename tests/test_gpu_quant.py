@@ -237,3 +237,13 @@ def test_scale_of_every_bf16_max_abs(oracle, pow2):
     torch.cuda.synchronize()
     assert_bytes_equal(u8(qT), qT_ref, "128x1 codes")
     assert_scales_equal(f32(sT), sT_ref, "128x1 scales")
+    # the fused 1x128 rows of the 128x1 quantiser: the same rows, padded with
+    # zero rows to a multiple of 128 tokens
+    T = (M + 127) // 128 * 128
+    xr = np.zeros((T, 128), np.uint16)
+    xr[:M] = x
+    qr_ref, sr_ref = oracle.quant_act(xr, pow2)
+    _, _, qr, sr = B.fp8q_quant_act_T(bf16_to_torch(xr), scale_mode=_mode(pow2), with_rows=True)
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(qr), qr_ref, "fused 1x128 codes")
+    assert_scales_equal(f32(sr), sr_ref, "fused 1x128 scales")
