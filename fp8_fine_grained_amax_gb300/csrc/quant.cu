@@ -462,8 +462,10 @@ __global__ void __launch_bounds__(kRqThreads, 4) requant_act_T_kernel(
       }
     }
 
-    // this thread: channel cw, tokens 8m + 2(lane%4), +1 (m = 0..15)
-    float x[32];
+    // this thread: channel cw, tokens 8m + 2(lane%4), +1 (m = 0..15); x2[m]
+    // holds the pair as packed FP32 (one mul.rn.f32x2 by the two row scales)
+    uint64_t x2[16];
+    float amax = 0.0f;
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
       uint32_t r4[4];
@@ -471,14 +473,12 @@ __global__ void __launch_bounds__(kRqThreads, 4) requant_act_T_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int m = 4 * qd + e;
-        const float2 sr = *reinterpret_cast<const float2 *>(&srow[8 * m + 2 * (lane & 3)]);
-        x[2 * m] = __fmul_rn(f16_lo(r4[e]), sr.x);
-        x[2 * m + 1] = __fmul_rn(f16_hi(r4[e]), sr.y);
+        const uint64_t sr = *reinterpret_cast<const uint64_t *>(&srow[8 * m + 2 * (lane & 3)]);
+        x2[m] = fmul2(pack_f32x2(f16_lo(r4[e]), f16_hi(r4[e])), sr);
+        const float2 xv = unpack_f32x2(x2[m]);
+        amax = fmaxf(amax, fmaxf(fabsf(xv.x), fabsf(xv.y)));
       }
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     float sc, inv;
@@ -488,11 +488,14 @@ __global__ void __launch_bounds__(kRqThreads, 4) requant_act_T_kernel(
     if (tid == 0) bulk_wait_group_read<1>();  // stage `buf`: its store two tiles ago has read it
     __syncthreads();  // every thread is done with the FP16 tile and row scales
     const uint32_t stg = st0 + buf * kRqStageBytes;
+    const uint64_t inv2 = pack_f32x2(inv, inv);
 #pragma unroll
-    for (int m = 0; m < 16; ++m)
+    for (int m = 0; m < 16; ++m) {
+      const float2 p = unpack_f32x2(fmul2(x2[m], inv2));
       st_shared_u16(stg + swz128(static_cast<uint32_t>(cw), static_cast<uint32_t>(m >> 1)) +
                         8u * (m & 1) + 2u * (lane & 3),
-                    pack_e4m3x2(__fmul_rn(x[2 * m], inv), __fmul_rn(x[2 * m + 1], inv)));
+                    pack_e4m3x2(p.x, p.y));
+    }
     fence_proxy_async_shared();
     __syncthreads();
     if (tid == 0) {
