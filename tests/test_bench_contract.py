@@ -124,6 +124,11 @@ def test_our_arm_json_line_on_the_gpu():
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     assert d["clocks"]["samples"] >= 1, d["clocks"]
     assert "workloads" not in d                  # only the headline run measures them all
+    # the timed loop is a replayed CUDA graph, and the per-kernel intervals
+    # (timing events on a side stream at every kernel boundary) cover the step
+    assert d["timing"]["mode"] == "cuda_graph", d["timing"]
+    kms = sum(v["ms"] for v in d["kernels"].values() if isinstance(v, dict))
+    assert 0.8 * d["ms_per_step"] <= kms <= 1.05 * d["ms_per_step"], (kms, d["ms_per_step"])
 
 
 @pytest.mark.parametrize("name", [n for _, n in __import__("bench").CONFIG_WORKLOADS] +
@@ -135,6 +140,20 @@ def test_every_configured_workload_is_known(name):
     wl = bench.make_workload(name)
     assert wl.name == name
     assert wl.work() > 0
+
+
+def test_buffer_copies_rotate_inputs_under_twice_the_l2():
+    # one copy only when a step's inputs alone exceed twice the L2; otherwise
+    # enough copies that the inputs read between two uses of a copy exceed
+    # twice the L2 (the Fprop step's 161 MB needs three)
+    import bench
+    L2 = bench.L2_BYTES
+    assert bench.buffer_copies(2 * L2 + 1) == 1
+    assert bench.buffer_copies(161 << 20) == 3
+    for n in (1 << 20, 58 << 20, L2, 2 * L2):
+        c = bench.buffer_copies(n)
+        assert c == min(bench.MAX_COPIES, -(-2 * L2 // n) + 1)
+        assert (c - 1) * n >= 2 * L2 or c == bench.MAX_COPIES
 
 
 def test_quant_weight_names():
