@@ -778,10 +778,10 @@ def make_workload(name: str) -> Workload:
 def workload_config(wl: Workload, in_bytes: int, world: int):
     """The line's `config`: the same dict for both arms of one workload."""
     n = buffer_copies(in_bytes)
-    l2 = (f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step > "
-          f"{L2_BYTES / 1e6:.0f} MB); no flush" if n == 1 else
-          f"inputs {in_bytes / 1e6:.1f} MB fit in L2: steps cycle through {n} copies of the "
-          f"step's buffers ({n * in_bytes / 1e6:.0f} MB of inputs); no flush")
+    l2 = (f"inputs larger than twice the L2 ({in_bytes / 1e6:.0f} MB read per step > "
+          f"2 x {L2_BYTES / 1e6:.0f} MB); no flush" if n == 1 else
+          f"inputs {in_bytes / 1e6:.1f} MB, under twice the L2: steps cycle through {n} "
+          f"copies of the step's buffers ({n * in_bytes / 1e6:.0f} MB of inputs); no flush")
     return dict(workload=wl.name, **wl.config, l2=l2, parallelism=f"replicas x{world}")
 
 
@@ -840,7 +840,7 @@ class Timer:
     """The K-step loop of one workload, repeated `repeats` times; each repeat
     sits between a barrier and a device synchronise.  `ks_sets` holds one
     kernel list per copy of the step's buffers; step i runs on copy
-    i % len(ks_sets), so that a workload whose inputs would fit in L2 reads
+    i % len(ks_sets), so that a workload whose inputs are under twice the L2 reads
     them from HBM (each copy has been evicted by the others by the time it
     comes round again).
 
