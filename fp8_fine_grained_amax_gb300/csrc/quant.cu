@@ -185,9 +185,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
 }
 
 // ------------------------------------------------------------------ tiles
-// The tile quantisers below (128x1, 128x1 from FP8, 128x128) work on 128 x 128
-// tiles with 512 threads (16 warps); row-wise work gives a half-warp to each
-// 256-byte row, four rows per thread.
+// The BF16 tile quantisers below (128x1 and 128x128) work on 128 x 128 tiles
+// with 512 threads (16 warps); the requantiser from FP8 uses 128 x 64 tiles
+// with 256 threads (its own constants).
 constexpr int kTileThreads = 512;
 
 // ------------------------------------------------------------------ 128x1
@@ -204,7 +204,8 @@ constexpr int kTileThreads = 512;
 //  - Codes go to a swizzled shared-memory copy of the transposed tile
 //    (channel rows of 128 bytes) that one TMA store writes out, so the
 //    transposed output costs no per-thread global stores.
-//  - Optionally the 1x128 codes of each token row (half-warp per row).
+//  - Optionally the 1x128 codes of each token row (eight lanes per row, 32
+//    bytes each).
 // Channels past C are zero-filled by TMA and clipped by the TMA store.
 constexpr uint32_t kTileBytesBF16 = 128 * 128 * 2;
 constexpr uint32_t kHalfBytesBF16 = kTileBytesBF16 / 2;   // 128 tokens x 64 channels
