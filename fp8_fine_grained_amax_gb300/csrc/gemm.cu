@@ -300,6 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;        // TMEM lanes this warp may access
     const int col_base = (ew >> 2) * kEpiCols;  // this warp's columns of the 256
     const int row_in_tile = static_cast<int>(rank) * BM + quarter * 32 + lane;
+    // Per-column scales: the partial is read in 16-lane x 8-column fragments,
+    // so that a thread needs the scales of 32 columns per K-group instead of
+    // 128 (shared-memory reads of the column scales bound the fold otherwise).
+    // Thread (g, q) = (lane / 4, lane % 4) holds rows g, g+8, g+16, g+24 of the
+    // warp's 32 and columns 8i + 2q, 8i + 2q + 1 (i = 0..15) of its 128, as
+    // acc[4i + r].  FP32 results leave straight from the fragments (the four
+    // lanes of a quad write 32 contiguous bytes of a row); BF16 results go back
+    // to one row per thread through shared memory first.
+    constexpr bool kFrag = kBScale == FP8Q_BSCALE_ROW;
+    const int g8 = lane >> 2, q4 = lane & 3;
+    const int fr[4] = {g8, g8 + 8, g8 + 16, g8 + 24};
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int NB = (p.N + 127) / 128;
     // the TMEM-empty barriers live in the MMA-issuing CTA
@@ -318,9 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nb = ncol0 / 128;
       const float *sb_g = p.sb;
       if (kGrouped) sb_g += static_cast<int64_t>(tl.g) * NB * p.num_kb;
-      // Scales of K-group kb: sa of this row; sb of this warp's columns (block
-      // kinds: one value; per-column kind: lane l holds the 4 scales of
-      // columns 4l..4l+3 of the warp's kEpiCols, staged in shared memory).
+      // Scales of K-group kb: sa of this lane's row (per-column kind: each
+      // thread takes its four rows' scales from their lanes by shuffles); sb
+      // of this warp's columns (block kinds: one value; per-column kind: lane
+      // l loads the scales of columns c, c+1, c+8, c+9, c = 16(l % 8) + 2(l / 8),
+      // and stores them at 4l..4l+3 of the warp's shared-memory row, so that
+      // thread (g, q) finds the 32 scales of its columns at 32q..32q+31).
       // Pointers to group 0's values advance by one group's stride per group;
       // rows past M, blocks past N and columns past N read as 0.
       const bool sa_in = m < p.M;
@@ -330,9 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           kBScale == FP8Q_BSCALE_BLOCK
               ? sb_g + static_cast<int64_t>(sb_in ? nb : 0) * (kGrouped ? p.num_kb : p.ld_sb)
           : kBScale == FP8Q_BSCALE_BLOCK_T ? p.sb + (sb_in ? nb : 0)
-                                           : p.sb + ncol0 + 4 * lane;
+                                           : p.sb + ncol0 + 16 * (lane & 7) + 2 * (lane >> 3);
       const int64_t sb_step = kBScale == FP8Q_BSCALE_BLOCK ? 1 : p.ld_sb;
-      const int ncol = ncol0 + 4 * lane;  // per-column kind: this lane's first column
+      // per-column kind: this lane's first column
+      const int ncol = ncol0 + 16 * (lane & 7) + 2 * (lane >> 3);
       auto load_sa = [&]() { return sa_in ? __ldg(sa_ptr) : 0.0f; };
       auto load_sb = [&]() {
         return kBScale != FP8Q_BSCALE_ROW && sb_in ? __ldg(sb_ptr) : 0.0f;
@@ -342,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kBScale == FP8Q_BSCALE_ROW) {
           if (ncol + 0 < p.N) v.x = __ldg(sb_ptr + 0);
           if (ncol + 1 < p.N) v.y = __ldg(sb_ptr + 1);
-          if (ncol + 2 < p.N) v.z = __ldg(sb_ptr + 2);
-          if (ncol + 3 < p.N) v.w = __ldg(sb_ptr + 3);
+          if (ncol + 8 < p.N) v.z = __ldg(sb_ptr + 8);
+          if (ncol + 9 < p.N) v.w = __ldg(sb_ptr + 9);
         }
         return v;
       };
@@ -373,7 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         const uint64_t scale2 = pack_f32x2(sa_v * sb_v, sa_v * sb_v);
-        const uint64_t sa2 = pack_f32x2(sa_v, sa_v);
+        uint64_t sa2f[4];  // per-column kind: this thread's four row scales, packed twice
+        if (kFrag) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float v = __shfl_sync(0xffffffffu, sa_v, fr[r]);
+            sa2f[r] = pack_f32x2(v, v);
+          }
+        }
         const bool got = mbar_wait_bounded(smem_u32(&ctl->tfull[tb]), tphase, abort_flag,
                                            &g_status, p.timeout_ns, FP8Q_ERR_TIMEOUT);
         if (!__all_sync(0xffffffffu, got)) {  // tcgen05.ld below needs the whole warp
@@ -382,35 +404,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(tb * BN + col_base);
-        // TMEM loads in flight per wait: four for per-column scales, whose fold
-        // has more arithmetic per column to overlap with the next loads
-        constexpr int kLdBatch = kBScale == FP8Q_BSCALE_ROW ? 4 : 1;
-        uint32_t rbuf[kLdBatch][16];
+        if (kFrag) {
+          // this thread's 32 column scales, eight per 32-column chunk
+          const uint32_t sbw = smem_u32(&ctl->sb_warp[ew][sb_iter & 1][q4 * 32]);
 #pragma unroll
-        for (int ch = 0; ch < kEpiCols / 16; ++ch) {
-          uint32_t(&r)[16] = rbuf[ch % kLdBatch];
-          if (kLdBatch == 1) {
+          for (int c = 0; c < kEpiCols / 32; ++c) {
+            uint32_t ra[16], rb[16];  // rows g, g+8 and g+16, g+24; columns 32c + 8k + 2q, +1
+            tmem_ld_16x256b_x4(taddr + c * 32, ra);
+            tmem_ld_16x256b_x4(taddr + (16u << 16) + c * 32, rb);
+            tmem_wait_ld_tied(ra);
+            reg_tie(rb);
+            const uint4 s0 = ld_shared_v4(sbw + c * 32), s1 = ld_shared_v4(sbw + c * 32 + 16);
+            const uint64_t sp[4] = {pack_u32x2(s0.x, s0.y), pack_u32x2(s0.z, s0.w),
+                                    pack_u32x2(s1.x, s1.y), pack_u32x2(s1.z, s1.w)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int i = 4 * c + k;
+              ffma2(acc[4 * i + 0], pack_u32x2(ra[4 * k], ra[4 * k + 1]), fmul2(sp[k], sa2f[0]));
+              ffma2(acc[4 * i + 1], pack_u32x2(ra[4 * k + 2], ra[4 * k + 3]), fmul2(sp[k], sa2f[1]));
+              ffma2(acc[4 * i + 2], pack_u32x2(rb[4 * k], rb[4 * k + 1]), fmul2(sp[k], sa2f[2]));
+              ffma2(acc[4 * i + 3], pack_u32x2(rb[4 * k + 2], rb[4 * k + 3]), fmul2(sp[k], sa2f[3]));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < kEpiCols / 16; ++ch) {
+            uint32_t r[16];
             tmem_ld_32x32b_x16(taddr + ch * 16, r);
             tmem_wait_ld();
-          } else if (ch % kLdBatch == 0) {
-#pragma unroll
-            for (int b = 0; b < kLdBatch; ++b) tmem_ld_32x32b_x16(taddr + (ch + b) * 16, rbuf[b]);
-            tmem_wait_ld_tied(rbuf[0]);
-#pragma unroll
-            for (int b = 1; b < kLdBatch; ++b) reg_tie(rbuf[b]);
-          }
-          if (kBScale == FP8Q_BSCALE_ROW) {
-            // 16-byte shared loads: four column scales per broadcast read
-            const ulonglong2 *sbr =
-                reinterpret_cast<const ulonglong2 *>(&ctl->sb_warp[ew][sb_iter & 1][ch * 16]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const ulonglong2 sp = sbr[j];
-              ffma2(acc[ch * 8 + 2 * j], pack_u32x2(r[4 * j], r[4 * j + 1]), fmul2(sp.x, sa2));
-              ffma2(acc[ch * 8 + 2 * j + 1], pack_u32x2(r[4 * j + 2], r[4 * j + 3]),
-                    fmul2(sp.y, sa2));
-            }
-          } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               ffma2(acc[ch * 8 + j], pack_u32x2(r[2 * j], r[2 * j + 1]), scale2);
@@ -427,6 +448,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++sb_iter;
       }
       if (!ok) break;
+
+      if (kFrag && kOutF32 && !kGrouped) {
+        // FP32 straight from the fragments: for each (i, r) the four lanes of a
+        // quad write 32 contiguous bytes of one row (8 rows per instruction)
+        const uint64_t pol = l2_evict_first_policy();
+        const int wrow = tl.a_row + static_cast<int>(rank) * BM + quarter * 32;
+#pragma unroll
+        for (int i = 0; i < kEpiCols / 8; ++i) {
+          const int col = ncol0 + 8 * i + 2 * q4;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = wrow + fr[r];
+            if (row >= tl.row_end || col >= p.N) continue;
+            float *dst = static_cast<float *>(p.c) + static_cast<int64_t>(row) * p.ldc + col;
+            float2 v = unpack_f32x2(acc[4 * i + r]);
+            if (col + 1 < p.N) {
+              if (kAccum) {
+                const float2 o = *reinterpret_cast<const float2 *>(dst);
+                v.x = __fadd_rn(o.x, v.x);
+                v.y = __fadd_rn(o.y, v.y);
+              }
+              st_global_b64_hint(dst, pack_f32x2(v.x, v.y), pol);
+            } else {
+              dst[0] = kAccum ? __fadd_rn(dst[0], v.x) : v.x;
+            }
+          }
+        }
+        continue;
+      }
+      if (kFrag) {
+        // BF16: fragments -> one row per thread, 64 columns at a time, through
+        // the warp's staging buffer (16-byte units XOR-swizzled by row), then
+        // the row-per-thread store below
+        const uint32_t buf = smem_u32(sC) + static_cast<uint32_t>(ew) * kStageWarpBytes;
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores have read it
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t unit = static_cast<uint32_t>(2 * i + (q4 >> 1));
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const uint32_t row = static_cast<uint32_t>(fr[r]);
+              st_shared_b64(buf + row * 256 + 16 * (unit ^ (row & 7)) + 8 * (q4 & 1),
+                            acc[4 * (8 * h + i) + r]);
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const uint4 v = ld_shared_v4(buf + lane * 256 + 16 * (u ^ (lane & 7)));
+            acc[32 * h + 2 * u] = pack_u32x2(v.x, v.y);
+            acc[32 * h + 2 * u + 1] = pack_u32x2(v.z, v.w);
+          }
+          __syncwarp();
+        }
+      }
 
       // ---- store this warp's 32 rows x kEpiCols columns
       // BF16 (dense with N a multiple of 8, and grouped): the whole block goes
