@@ -118,6 +118,37 @@ def test_gemm_wgrad_row_scales(oracle, out):
     _check(c, ref, ad, out == "bf16", "wgrad")
 
 
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_gemm_wgrad_row_scales_odd_n(oracle, out):
+    # per-column scales with an odd N: the FP32 fragments end in a lone
+    # column (scalar store) and BF16 rows end inside a 16-byte unit (row
+    # stores, no tensor store); C is a strided view whose padding columns
+    # must stay untouched
+    T, d_in, d_out = 256, 101, 264
+    dy = synth.normal_bf16((T, d_out), 1e-3, 7, "wgrad.dY.odd")
+    x = synth.activation(T, d_in, seed=8, name="wgrad.X.odd")
+    xpad = torch.zeros((T, 104), dtype=torch.bfloat16, device="cuda")
+    xpad[:, :d_in] = bf16_to_torch(x)
+    qdyT, sdyT = B.fp8q_quant_act_T(bf16_to_torch(dy))
+    # channels are quantised independently: the first 101 of the padded X's
+    # 104 are X's own (the 128x1 quantiser takes C in multiples of 8)
+    qxT_full, sxT_full = B.fp8q_quant_act_T(xpad)
+    qxT, sxT = qxT_full[:d_in], sxT_full[:, :d_in]
+    fp32 = out == "fp32"
+    od = B.FP8Q_OUT_FP32 if fp32 else B.FP8Q_OUT_BF16
+    cbuf = torch.full((d_out, 104), 7.0, dtype=torch.float32 if fp32 else torch.bfloat16,
+                      device="cuda")
+    B.fp8q_gemm(qdyT, sdyT, qxT, sxT, bscale_kind=B.FP8Q_BSCALE_ROW, out_dtype=od,
+                c=cbuf[:, :d_in])
+    torch.cuda.synchronize()
+    qdyT_r, sdyT_r = oracle.quant_act_T(dy)
+    qxT_r, sxT_r = oracle.quant_act_T(x)
+    assert_bytes_equal(u8(qxT), qxT_r, "X^T codes")
+    ref, ad = oracle.gemm_rows(qdyT_r, sdyT_r, qxT_r, sxT_r, oracle.BSCALE_ROW)
+    _check(cbuf[:, :d_in], ref, ad, not fp32, "wgrad, odd N")
+    assert bool((cbuf[:, d_in:] == 7.0).all()), "padding columns written"
+
+
 def test_gemm_k_zero_writes_zeros():
     M, N = 130, 264
     a = torch.empty((M, 0), dtype=torch.uint8, device="cuda")
