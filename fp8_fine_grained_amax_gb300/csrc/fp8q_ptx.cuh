@@ -152,6 +152,20 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t smem_row_addr, uint32
                : "memory");
 }
 
+// Two 16x16 byte matrices from shared memory, transposed: lanes 16i..16i+15
+// give the addresses of the 16 rows (16 bytes each) of matrix i; lane 4g + t
+// receives, for matrix i, rows 4t..4t+3 of column g in the bytes of
+// r[2i] (row 4t in the low byte) and the same rows of column g + 8 in r[2i+1].
+__device__ __forceinline__ void ldmatrix_b8_x2_trans(uint32_t smem_row_addr, uint32_t *r) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_row_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
 }

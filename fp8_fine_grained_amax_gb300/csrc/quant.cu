@@ -221,60 +221,67 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
     int64_t C, float *__restrict__ sT, int64_t ld_sT, uint8_t *__restrict__ q_rows,
     int64_t ldq_rows, float *__restrict__ s_rows, int64_t ld_s_rows, uint64_t timeout_ns) {
   extern __shared__ uint8_t dsm_raw[];
-  uint8_t *base = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t in0 = smem_u32(base);                    // 2 x 32 KB input tiles
-  const uint32_t st0 = in0 + 2 * kTileBytesBF16;          // 2 x 16 KB staged codes
+  const uint32_t in0 = (smem_u32(dsm_raw) + 1023u) & ~1023u;  // 2 x 32 KB input tiles
+  const uint32_t st0 = in0 + 2 * kTileBytesBF16;               // 2 x 16 KB staged codes
   __shared__ uint64_t full[2];
+  __shared__ uint32_t consumed[2];  // warps done with the buffer's current tile
+  __shared__ int pending[2];        // parity of the last copy issued per buffer, or -1
   __shared__ int abort_flag;
   __shared__ ScaleTables tabs;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr uint32_t kWarps = kTileThreads / 32;
   scale_tables_init(tabs, tid);  // visible after the __syncthreads below
-  const int64_t ncb = (C + 127) / 128;
-  const int64_t ntiles = ncb * (T / 128);
-  int pending[2] = {-1, -1};  // thread 0: parity of the copy in flight per buffer
-  auto issue_load = [&](int b, int64_t t) {
+  // tile t = (token block t / ncb, channel block t % ncb); this CTA takes
+  // t = blockIdx.x + i * gridDim.x, walked incrementally
+  const uint32_t ncb = static_cast<uint32_t>((C + 127) / 128), ntb = static_cast<uint32_t>(T / 128);
+  const uint32_t dcb = gridDim.x % ncb, dtb = gridDim.x / ncb;
+  auto step = [&](uint32_t &cb, uint32_t &tb) {
+    cb += dcb;
+    tb += dtb;
+    if (cb >= ncb) {
+      cb -= ncb;
+      ++tb;
+    }
+  };
+  auto issue_load = [&](int b, uint32_t cb, uint32_t tb) {
     const uint32_t bar = smem_u32(&full[b]);
     mbar_arrive_expect_tx(bar, kTileBytesBF16);
-    const int32_t c0 = static_cast<int32_t>((t % ncb) * 128), t0 = static_cast<int32_t>((t / ncb) * 128);
+    const int32_t c0 = static_cast<int32_t>(cb * 128), t0 = static_cast<int32_t>(tb * 128);
     tma_load_2d(in0 + b * kTileBytesBF16, &tmX, bar, c0, t0);
     tma_load_2d(in0 + b * kTileBytesBF16 + kHalfBytesBF16, &tmX, bar, c0 + 64, t0);
   };
+  uint32_t cb = blockIdx.x % ncb, tb = blockIdx.x / ncb;  // this tile
+  uint32_t cbn = cb, tbn = tb;                            // the tile two ahead
   if (tid == 0) {
-    mbar_init(smem_u32(&full[0]), 1);
-    mbar_init(smem_u32(&full[1]), 1);
     abort_flag = 0;
-    fence_barrier_init();
     for (int b = 0; b < 2; ++b) {
-      const int64_t t = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
-      if (t < ntiles) {
-        issue_load(b, t);
-        pending[b] = 0;
-      }
+      mbar_init(smem_u32(&full[b]), 1);
+      consumed[b] = 0;
+      pending[b] = -1;
     }
+    fence_barrier_init();
+  }
+  for (int b = 0; b < 2; ++b) {
+    if (tid == 0 && tbn < ntb) {
+      issue_load(b, cbn, tbn);
+      pending[b] = 0;
+    }
+    step(cbn, tbn);
   }
   __syncthreads();
 
   // this warp's channels: half h, 16-byte chunk j of each token row
   const uint32_t h = static_cast<uint32_t>(warp >> 3), j = static_cast<uint32_t>(warp & 7);
   const int cw = 8 * warp + (lane >> 2);  // this thread's channel within the tile
-  int it = 0;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-    const int buf = it & 1;
-    const bool got = mbar_wait_bounded(smem_u32(&full[buf]), (it >> 1) & 1, &abort_flag,
+  int buf = 0;
+  uint32_t phase = 0;
+  while (tb < ntb) {
+    const bool got = mbar_wait_bounded(smem_u32(&full[buf]), phase, &abort_flag,
                                        &g_quant_status, timeout_ns, FP8Q_ERR_TIMEOUT);
-    if (__syncthreads_or(!got)) {
-      if (tid == 0) {  // let this CTA's own copies land before it exits
-        for (int b = 0; b < 2; ++b)
-          if (pending[b] >= 0) mbar_wait_drain(smem_u32(&full[b]), pending[b]);
-        bulk_wait_group_all();
-      }
-      return;
-    }
-    if (tid == 0) pending[buf] = -1;
+    if (__any_sync(0xffffffffu, !got)) break;
     const uint32_t tin = in0 + buf * kTileBytesBF16;
-    const int64_t c0 = (t % ncb) * 128, t0 = (t / ncb) * 128;
+    const int64_t c0 = static_cast<int64_t>(cb) * 128, t0 = static_cast<int64_t>(tb) * 128;
 
     if (kRows) {  // C % 128 == 0 here: every chunk is in range
       // eight lanes per token row, 16 channels (two 16-byte chunks) each
@@ -312,6 +319,25 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) v[4 * qd + e] = r4[e];
     }
+    __syncwarp();  // the warp's reads of buffer `buf` are done
+    if (lane == 0) {
+      uint32_t prev;
+      asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "r"(smem_u32(&consumed[buf]))
+                   : "memory");
+      if (prev == kWarps - 1) {  // the last reader refills the buffer
+        consumed[buf] = 0;
+        if (tbn < ntb) {
+          fence_proxy_async_shared();  // generic-proxy reads above, async-proxy write below
+          pending[buf] = static_cast<int>(phase ^ 1u);
+          issue_load(buf, cbn, tbn);
+        }
+      }
+    }
+    step(cb, tb);
+    step(cbn, tbn);
+
     uint32_t mw = 0;
 #pragma unroll
     for (int m = 0; m < 16; ++m) mw = umax16x2(mw, v[m] & 0x7FFF7FFFu);
@@ -325,32 +351,32 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 #pragma unroll
     for (int m = 0; m < 16; ++m) code[m] = quantise2(v[m], inv2);
 
-    // the staged codes written two tiles ago must have been read by their store
-    if (tid == 0) bulk_wait_group_read<1>();
-    __syncthreads();  // every thread is done with input buffer `buf` and may reuse stage `buf`
-    if (tid == 0) {
-      const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
-      if (tn < ntiles) {
-        // generic-proxy reads of the buffer above, async-proxy write below
-        fence_proxy_async_shared();
-        issue_load(buf, tn);
-        pending[buf] = ((it + 2) >> 1) & 1;
-      }
-    }
-    const uint32_t stg = st0 + buf * kTileBytesQ;
+    // this warp's 8 channel rows (1 KB) of the staged transposed tile; its
+    // store two tiles ago must have read them
+    const uint32_t stg = st0 + buf * kTileBytesQ + static_cast<uint32_t>(warp) * 1024u;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
 #pragma unroll
     for (int m = 0; m < 16; ++m)
-      st_shared_u16(stg + swz128(static_cast<uint32_t>(cw), static_cast<uint32_t>(m >> 1)) +
+      st_shared_u16(stg + swz128(static_cast<uint32_t>(lane >> 2), static_cast<uint32_t>(m >> 1)) +
                         8u * (m & 1) + 2u * (lane & 3),
                     code[m]);
     fence_proxy_async_shared();
-    __syncthreads();
-    if (tid == 0) {
-      tma_store_2d(&tmQ, stg, static_cast<int32_t>(t0), static_cast<int32_t>(c0));
+    __syncwarp();
+    if (lane == 0 && c0 + 8 * warp < C) {  // C % 8 == 0: the 8 rows are all in range or all out
+      tma_store_2d(&tmQ, stg, static_cast<int32_t>(t0), static_cast<int32_t>(c0 + 8 * warp));
       bulk_commit_group();
     }
+    buf ^= 1;
+    if (buf == 0) phase ^= 1u;
   }
-  if (tid == 0) bulk_wait_group_all();
+  // every warp has left the loop (all tiles done, or a wait gave up): copies
+  // still in flight after an abort land before the CTA's shared memory goes
+  __syncthreads();
+  if (tid == 0 && abort_flag)
+    for (int b = 0; b < 2; ++b)
+      if (pending[b] >= 0) mbar_wait_drain(smem_u32(&full[b]), static_cast<uint32_t>(pending[b]));
+  if (lane == 0) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ 128x1 from FP8
@@ -358,153 +384,199 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 // activations: input E4M3 [T][C] with one 1x128 scale per (token, 128
 // channels), output the 128x1 codes transposed.  Each value is first
 // dequantised with one FP32 multiply, x = fl32(decode(q) * s_row), exactly as a
-// BF16 input would be read.  Per tile: the raw codes arrive by TMA (two-deep
-// ring); they are decoded exactly (E4M3 is a subset of FP16) into a
-// 128-byte-swizzled FP16 tile; ldmatrix.trans reads it by channel; the
-// transposed codes leave through one TMA store.  The next tile's row scales
-// are loaded while this one is processed.  Tiles are 128 tokens x 64 channels
-// (a 64-channel tile lies inside one 128-channel group of the row scales), so
-// that a CTA needs 48 KB of shared memory and four CTAs share an SM: the
-// decode, reduce and store phases of a tile are separated by CTA barriers,
-// and other CTAs' phases fill the gaps.  Warp w of 8 owns channels 8w..8w+7.
-constexpr int kRqCh = 64;                                  // channels per tile
+// BF16 input would be read.
+//  - Tiles of 128 tokens x 128 channels (one row-scale group), channel blocks
+//    fastest; the raw codes arrive by TMA in a three-deep ring, 128-byte
+//    swizzled (16-byte chunk k of token row r at chunk k ^ (r % 8)).
+//  - Warp w owns channels 16w..16w+15.  Four byte-wise ldmatrix.trans give
+//    lane 4g + t the codes of tokens 32p + 16h + 4t + {0..3} (p = 0..3,
+//    h = 0..1) of channels g and g + 8, four tokens of one channel per
+//    register: the codes are transposed as bytes, and decoding, scaling, the
+//    channel max-abs (two shuffles) and the new codes all happen in registers
+//    in the transposed orientation.
+//  - Each warp stages its 16 channel rows of new codes (128-byte swizzle,
+//    conflict-free 32-bit stores) and writes them with its own TMA store.
+//  - No CTA barrier in the loop: each warp keeps its own copy of the row
+//    scales (loaded one tile ahead), and the last warp to finish reading an
+//    input stage refills it (a shared counter with acquire-release order).
 constexpr int kRqThreads = 256;
-constexpr uint32_t kRqRawBytes = 128 * kRqCh;              // raw codes, 64-byte rows
-constexpr uint32_t kRqF16Bytes = 128 * kRqCh * 2;          // FP16 tile, 128-byte rows
-constexpr uint32_t kRqStageBytes = kRqCh * 128;            // transposed codes
+constexpr int kRqWarps = kRqThreads / 32;
+constexpr int kRqStages = 3;
+constexpr int kRqCtasPerSm = 2;
+constexpr uint32_t kRqTileBytes = 128 * 128;   // raw codes, 128-byte token rows
+constexpr uint32_t kRqStripBytes = 16 * 128;   // one warp's 16 rows of new codes
 template <bool kPow2>
-__global__ void __launch_bounds__(kRqThreads, 4) requant_act_T_kernel(
+__global__ void __launch_bounds__(kRqThreads, kRqCtasPerSm) requant_act_T_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQT, int64_t T,
     int64_t C, const float *__restrict__ s_rows, int64_t ld_s_rows, float *__restrict__ sT,
     int64_t ld_sT, uint64_t timeout_ns) {
   extern __shared__ uint8_t dsm_raw[];
-  __shared__ __align__(16) float srow[128];
-  __shared__ uint64_t full[2];
+  __shared__ __align__(16) float srow[kRqWarps][2][128];
+  __shared__ uint64_t full[kRqStages];
+  __shared__ uint32_t consumed[kRqStages];  // warps done with the stage's current tile
+  __shared__ int pending[kRqStages];        // parity of the last copy issued per stage, or -1
   __shared__ int abort_flag;
-  const uint32_t raw0 = (smem_u32(dsm_raw) + 1023u) & ~1023u;  // 2 x 8 KB raw codes
-  const uint32_t tin = raw0 + 2 * kRqRawBytes;                // 16 KB FP16 tile
-  const uint32_t st0 = tin + kRqF16Bytes;                      // 2 x 8 KB staged codes
+  const uint32_t raw0 = (smem_u32(dsm_raw) + 1023u) & ~1023u;  // kRqStages x 16 KB
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  // two 2 KB strips of staged codes per warp
+  const uint32_t strip0 = raw0 + kRqStages * kRqTileBytes + warp * 2 * kRqStripBytes;
 
-  const int tid = threadIdx.x, hw = tid >> 3, l8 = tid & 7;
-  const int64_t ncb = C / kRqCh;
-  const int64_t ntiles = ncb * (T / 128);
-  int pending[2] = {-1, -1};
-  auto issue_load = [&](int b, int64_t t) {
-    const uint32_t bar = smem_u32(&full[b]);
-    mbar_arrive_expect_tx(bar, kRqRawBytes);
-    tma_load_2d(raw0 + b * kRqRawBytes, &tmQ, bar, static_cast<int32_t>((t % ncb) * kRqCh),
-                static_cast<int32_t>((t / ncb) * 128));
-  };
-  auto row_scale = [&](int64_t t) {  // threads < 128: this tile's scale of token row tid
-    return s_rows[((t % ncb) * kRqCh / 128) * ld_s_rows + (t / ncb) * 128 + tid];
-  };
-  if (tid == 0) {
-    mbar_init(smem_u32(&full[0]), 1);
-    mbar_init(smem_u32(&full[1]), 1);
-    abort_flag = 0;
-    fence_barrier_init();
-    for (int b = 0; b < 2; ++b) {
-      const int64_t t = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
-      if (t < ntiles) {
-        issue_load(b, t);
-        pending[b] = 0;
-      }
+  // tile t = (token block t / ncb, channel block t % ncb); this CTA takes
+  // t = blockIdx.x + i * gridDim.x, walked incrementally
+  const uint32_t ncb = static_cast<uint32_t>(C / 128), ntb = static_cast<uint32_t>(T / 128);
+  const uint32_t dcb = gridDim.x % ncb, dtb = gridDim.x / ncb;
+  auto step = [&](uint32_t &cb, uint32_t &tb) {
+    cb += dcb;
+    tb += dtb;
+    if (cb >= ncb) {
+      cb -= ncb;
+      ++tb;
     }
+  };
+  auto issue_load = [&](int st, uint32_t cb, uint32_t tb) {
+    const uint32_t bar = smem_u32(&full[st]);
+    mbar_arrive_expect_tx(bar, kRqTileBytes);
+    tma_load_2d(raw0 + st * kRqTileBytes, &tmQ, bar, static_cast<int32_t>(cb * 128),
+                static_cast<int32_t>(tb * 128));
+  };
+  // lane l: the row scales of tokens l + 32i of tile (cb, tb)
+  auto load_scales = [&](uint32_t cb, uint32_t tb, float (&v)[4]) {
+    const float *p = s_rows + static_cast<int64_t>(cb) * ld_s_rows + tb * 128u + lane;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = p[32 * i];
+  };
+
+  uint32_t cb = blockIdx.x % ncb, tb = blockIdx.x / ncb;  // this tile
+  uint32_t cbn = cb, tbn = tb;                            // the tile kRqStages ahead
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int st = 0; st < kRqStages; ++st) {
+      mbar_init(smem_u32(&full[st]), 1);
+      consumed[st] = 0;
+      pending[st] = -1;
+    }
+    fence_barrier_init();
   }
-  float sr_next = 0.0f;
-  if (tid < 128 && static_cast<int64_t>(blockIdx.x) < ntiles) sr_next = row_scale(blockIdx.x);
+  for (int st = 0; st < kRqStages; ++st) {
+    if (tid == 0 && tbn < ntb) {
+      issue_load(st, cbn, tbn);
+      pending[st] = 0;
+    }
+    step(cbn, tbn);
+  }
+  float sn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (tb < ntb) load_scales(cb, tb, sn);
   __syncthreads();
 
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t j = static_cast<uint32_t>(warp);  // the warp's 16-byte chunk of each FP16 row
-  const int cw = 8 * warp + (lane >> 2);  // this thread's channel within the tile
-  int it = 0;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-    const int buf = it & 1;
-    const bool got = mbar_wait_bounded(smem_u32(&full[buf]), (it >> 1) & 1, &abort_flag,
+  // ldmatrix: lane l gives token row 32p + l, chunk `warp` of it (swizzled)
+  const uint32_t ld_off = static_cast<uint32_t>(lane) * 128u +
+                          ((static_cast<uint32_t>(warp) ^ (static_cast<uint32_t>(lane) & 7u)) << 4);
+  int st = 0;
+  uint32_t phase = 0, sb = 0;
+  while (tb < ntb) {
+    const bool got = mbar_wait_bounded(smem_u32(&full[st]), phase, &abort_flag,
                                        &g_quant_status, timeout_ns, FP8Q_ERR_TIMEOUT);
-    if (__syncthreads_or(!got)) {
-      if (tid == 0) {
-        for (int b = 0; b < 2; ++b)
-          if (pending[b] >= 0) mbar_wait_drain(smem_u32(&full[b]), pending[b]);
-        bulk_wait_group_all();
-      }
-      return;
-    }
-    if (tid == 0) pending[buf] = -1;
-    const int64_t c0 = (t % ncb) * kRqCh, t0 = (t / ncb) * 128;
-    if (tid < 128) {
-      srow[tid] = sr_next;
-      if (t + gridDim.x < ntiles) sr_next = row_scale(t + gridDim.x);
-    }
-    // decode: thread (hw, l8) takes 8 codes of token rows hw + 32 i
+    if (__any_sync(0xffffffffu, !got)) break;
+    // r[4p + 2h + j]: channel g + 8j, tokens 32p + 16h + 4tq + {0..3}
+    uint32_t r[16];
+    const uint32_t in = raw0 + st * kRqTileBytes;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t r = static_cast<uint32_t>(hw + 32 * i);
-      uint2 q8;
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                   : "=r"(q8.x), "=r"(q8.y)
-                   : "r"(raw0 + buf * kRqRawBytes + r * static_cast<uint32_t>(kRqCh) + 8u * l8));
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                       tin + swz128(r, static_cast<uint32_t>(l8))),
-                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.x & 0xFFFF))),
-                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.x >> 16))),
-                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.y & 0xFFFF))),
-                   "r"(decode_e4m3x2(static_cast<uint16_t>(q8.y >> 16)))
+    for (int p = 0; p < 4; ++p) ldmatrix_b8_x2_trans(in + 4096u * p + ld_off, &r[4 * p]);
+    float *srw = srow[warp][sb];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) srw[lane + 32 * i] = sn[i];
+    __syncwarp();  // the warp's reads of stage `st` are done; its row scales are visible
+    if (lane == 0) {
+      uint32_t prev;
+      asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "r"(smem_u32(&consumed[st]))
                    : "memory");
-    }
-    __syncthreads();  // FP16 tile and row scales ready; raw buffer `buf` consumed
-    if (tid == 0) {
-      const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
-      if (tn < ntiles) {
-        fence_proxy_async_shared();  // generic-proxy reads above, async-proxy write below
-        issue_load(buf, tn);
-        pending[buf] = ((it + 2) >> 1) & 1;
+      if (prev == kRqWarps - 1) {  // the last reader refills the stage
+        consumed[st] = 0;
+        if (tbn < ntb) {
+          fence_proxy_async_shared();  // generic-proxy reads above, async-proxy write below
+          pending[st] = static_cast<int>(phase ^ 1u);
+          issue_load(st, cbn, tbn);
+        }
       }
+    }
+    const uint32_t cbc = cb, tbc = tb;
+    step(cb, tb);
+    step(cbn, tbn);
+    if (tb < ntb) load_scales(cb, tb, sn);  // next tile's row scales, used one tile later
+    if (++st == kRqStages) {
+      st = 0;
+      phase ^= 1u;
     }
 
-    // this thread: channel cw, tokens 8m + 2(lane%4), +1 (m = 0..15); x2[m]
-    // holds the pair as packed FP32 (one mul.rn.f32x2 by the two row scales)
-    uint64_t x2[16];
-    float amax = 0.0f;
+    // decode and scale: x[2k], x[2k+1] are tokens {0,1} and {2,3} of r[k] as
+    // packed FP32 (one mul.rn.f32x2 by the pair of row scales)
+    uint64_t x[32];
+    float am0 = 0.0f, am1 = 0.0f;
 #pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-      uint32_t r4[4];
-      ldmatrix_x4_trans(tin + swz128(32u * qd + lane, j), r4);
+    for (int ph = 0; ph < 8; ++ph) {
+      const ulonglong2 sp = *reinterpret_cast<const ulonglong2 *>(&srw[16 * ph + 4 * tq]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int m = 4 * qd + e;
-        const uint64_t sr = *reinterpret_cast<const uint64_t *>(&srow[8 * m + 2 * (lane & 3)]);
-        x2[m] = fmul2(pack_f32x2(f16_lo(r4[e]), f16_hi(r4[e])), sr);
-        const float2 xv = unpack_f32x2(x2[m]);
-        amax = fmaxf(amax, fmaxf(fabsf(xv.x), fabsf(xv.y)));
+      for (int j = 0; j < 2; ++j) {
+        const int k = 2 * ph + j;
+        const uint32_t h01 = decode_e4m3x2(static_cast<uint16_t>(r[k] & 0xFFFFu));
+        const uint32_t h23 = decode_e4m3x2(static_cast<uint16_t>(r[k] >> 16));
+        x[2 * k] = fmul2(pack_f32x2(f16_lo(h01), f16_hi(h01)), sp.x);
+        x[2 * k + 1] = fmul2(pack_f32x2(f16_lo(h23), f16_hi(h23)), sp.y);
+        const float2 a = unpack_f32x2(x[2 * k]), b = unpack_f32x2(x[2 * k + 1]);
+        const float m = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
+        if (j == 0)
+          am0 = fmaxf(am0, m);
+        else
+          am1 = fmaxf(am1, m);
       }
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    sb ^= 1u;
+    am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, 1));
+    am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 1));
+    am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, 2));
+    am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 2));
+    // lanes tq < 2 take channel g's scale, tq >= 2 channel g + 8's; shuffles
+    // give every lane both inverses
     float sc, inv;
-    group_scale(amax, kPow2, sc, inv);
-    if ((lane & 3) == 0) sT[(t0 / 128) * ld_sT + c0 + cw] = sc;
+    group_scale(tq < 2 ? am0 : am1, kPow2, sc, inv);
+    if ((tq & 1) == 0) sT[static_cast<int64_t>(tbc) * ld_sT + cbc * 128u + 16 * warp + g + 4 * tq] = sc;
+    const float inv0 = __shfl_sync(0xffffffffu, inv, lane & ~3);
+    const float inv1 = __shfl_sync(0xffffffffu, inv, (lane & ~3) | 2);
+    const uint64_t iv[2] = {pack_f32x2(inv0, inv0), pack_f32x2(inv1, inv1)};
 
-    if (tid == 0) bulk_wait_group_read<1>();  // stage `buf`: its store two tiles ago has read it
-    __syncthreads();  // every thread is done with the FP16 tile and row scales
-    const uint32_t stg = st0 + buf * kRqStageBytes;
-    const uint64_t inv2 = pack_f32x2(inv, inv);
+    const uint32_t stg = strip0 + (sb ^ 1u) * kRqStripBytes;
+    if (lane == 0) bulk_wait_group_read<1>();  // this strip's store two tiles ago has read it
+    __syncwarp();
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float2 p = unpack_f32x2(fmul2(x2[m], inv2));
-      st_shared_u16(stg + swz128(static_cast<uint32_t>(cw), static_cast<uint32_t>(m >> 1)) +
-                        8u * (m & 1) + 2u * (lane & 3),
-                    pack_e4m3x2(p.x, p.y));
+    for (int ph = 0; ph < 8; ++ph) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int k = 2 * ph + j;
+        const float2 a = unpack_f32x2(fmul2(x[2 * k], iv[j]));
+        const float2 b = unpack_f32x2(fmul2(x[2 * k + 1], iv[j]));
+        // channel row g + 8j, token chunk ph (bytes 16ph + 4tq), swizzled by row % 8 = g
+        st_shared_u32(stg + static_cast<uint32_t>(g + 8 * j) * 128u +
+                          ((static_cast<uint32_t>(ph) ^ static_cast<uint32_t>(g)) << 4) + 4u * tq,
+                      pack_e4m3x4(a.x, a.y, b.x, b.y));
+      }
     }
     fence_proxy_async_shared();
-    __syncthreads();
-    if (tid == 0) {
-      tma_store_2d(&tmQT, stg, static_cast<int32_t>(t0), static_cast<int32_t>(c0));
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&tmQT, stg, static_cast<int32_t>(tbc * 128), static_cast<int32_t>(cbc * 128 + 16 * warp));
       bulk_commit_group();
     }
   }
-  if (tid == 0) bulk_wait_group_all();
+  // every warp has left the loop (all tiles done, or a wait gave up): copies
+  // still in flight after an abort land before the CTA's shared memory goes
+  __syncthreads();
+  if (tid == 0 && abort_flag)
+    for (int b = 0; b < kRqStages; ++b)
+      if (pending[b] >= 0) mbar_wait_drain(smem_u32(&full[b]), static_cast<uint32_t>(pending[b]));
+  if (lane == 0) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ 128x128
@@ -726,8 +798,8 @@ fp8q_status launch_act_T(unsigned grid, cudaStream_t s, const CUtensorMap &tmX,
                    q_rows, ldq_rows, s_rows, ld_s_rows, timeout_ns);
 }
 
-constexpr size_t kRequantSmem = 2 * kRqRawBytes + kRqF16Bytes + 2 * kRqStageBytes + 1024;
-constexpr int kRequantCtasPerSm = 4;
+constexpr size_t kRequantSmem =
+    kRqStages * kRqTileBytes + (kRqThreads / 32) * 2 * kRqStripBytes + 1024;
 
 template <bool kPow2>
 fp8q_status launch_requant(unsigned grid, cudaStream_t s, const CUtensorMap &tmQ,
@@ -811,7 +883,7 @@ extern "C" fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int
   if (T < 0 || C < 0 || T % 128 != 0 || C % 8 != 0 || ldx < C || ldqT < T || ld_sT < C)
     return FP8Q_ERR_SHAPE;
   if (rows && (C % 128 != 0 || ldq_rows < C || ld_s_rows < T)) return FP8Q_ERR_SHAPE;
-  if (T / 128 > 65535) return FP8Q_ERR_SHAPE;
+  if (T / 128 > 65535 || C > INT32_MAX - 127) return FP8Q_ERR_SHAPE;  // 32-bit tile coordinates
   if (T == 0 || C == 0) return FP8Q_OK;
   if (!x || !qT || !sT || (rows && !s_rows)) return FP8Q_ERR_INVALID;
   if (!aligned16(x) || !aligned16(qT) || !aligned4(sT) || ldx % 8 || ldqT % 16)
@@ -820,13 +892,14 @@ extern "C" fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
   // input: 64-channel x 128-token boxes, 128-byte swizzle; output: the
-  // transposed codes qT [C][T], 128-token x 128-channel boxes, same swizzle
+  // transposed codes qT [C][T], 128-token x 8-channel boxes (one warp's
+  // rows), same swizzle
   CUtensorMap tmX, tmQ;
   if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(T),
                     static_cast<uint64_t>(C), static_cast<uint64_t>(ldx) * 2, 64, 128,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, qT, static_cast<uint64_t>(C),
-                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, 128,
+                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, 8,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return FP8Q_ERR_CUDA;
   const int64_t ntiles = ((C + 127) / 128) * (T / 128);
@@ -908,7 +981,7 @@ extern "C" fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, i
   if (T < 0 || C < 0 || T % 128 != 0 || C % 128 != 0 || ldq < C || ld_s_rows < T || ldqT < T ||
       ld_sT < C)
     return FP8Q_ERR_SHAPE;
-  if (T / 128 > 65535) return FP8Q_ERR_SHAPE;
+  if (T / 128 > 65535 || C > INT32_MAX) return FP8Q_ERR_SHAPE;  // 32-bit tile coordinates
   if (T == 0 || C == 0) return FP8Q_OK;
   if (!q || !s_rows || !qT || !sT) return FP8Q_ERR_INVALID;
   if (!aligned16(q) || !aligned16(qT) || !aligned4(s_rows) || !aligned4(sT) || ldq % 16 ||
@@ -916,18 +989,18 @@ extern "C" fp8q_status fp8q_requant_act_T(const void *q, int64_t T, int64_t C, i
     return FP8Q_ERR_ALIGN;
   DeviceInfo dev;
   if (fp8q_status st = device_info(dev)) return st;
-  // codes [T][C] in boxes of 128 tokens x 64 bytes; qT [C][T] in boxes of 64
-  // channel rows x 128 bytes
+  // codes [T][C] in boxes of 128 tokens x 128 bytes; qT [C][T] in boxes of 16
+  // channel rows x 128 bytes (one warp's strip); both 128-byte swizzled
   CUtensorMap tmQ, tmQT;
   if (!make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, static_cast<uint64_t>(T),
-                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldq), kRqCh, 128,
-                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                    static_cast<uint64_t>(C), static_cast<uint64_t>(ldq), 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&tmQT, CU_TENSOR_MAP_DATA_TYPE_UINT8, qT, static_cast<uint64_t>(C),
-                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, kRqCh,
+                    static_cast<uint64_t>(T), static_cast<uint64_t>(ldqT), 128, 16,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return FP8Q_ERR_CUDA;
-  const int64_t ntiles = (C / kRqCh) * (T / 128);
-  const int64_t cap = static_cast<int64_t>(dev.sm_count) * kRequantCtasPerSm;
+  const int64_t ntiles = (C / 128) * (T / 128);
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * kRqCtasPerSm;
   const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
   auto s = static_cast<cudaStream_t>(stream);
   const uint64_t tmo = wait_timeout_ns().load();

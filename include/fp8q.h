@@ -114,7 +114,8 @@ fp8q_status fp8q_quant_act_T(const void *x, int64_t T, int64_t C, int64_t ldx,
  * same tensor in 128x1 tiles ([dssusan] paragraph 4).  Each cached value is
  * dequantised with one FP32 multiply, x = fl32(decode(q[t][c]) * s_rows(t, c)),
  * then quantised exactly as fp8q_quant_act_T quantises x.
- *   q       E4M3 [T][ldq], columns [0, C).          T % 128 == 0, C % 128 == 0.
+ *   q       E4M3 [T][ldq], columns [0, C).          T % 128 == 0, C % 128 == 0,
+ *           T <= 65535 * 128, C <= 2^31 - 1 (else FP8Q_ERR_SHAPE).
  *   s_rows  FP32 1x128 scales of q: s_rows[(c/128) * ld_s_rows + t], ld_s_rows >= T.
  *   qT      E4M3 [C][ldqT], qT[c][t];  sT FP32 sT[(t/128) * ld_sT + c].
  * Alignment: q, qT 16-byte aligned; ldq % 16 == 0, ldqT % 16 == 0.
