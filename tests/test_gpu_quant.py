@@ -92,7 +92,8 @@ def test_quant_act_T(oracle, T, C, rows, pow2):
 
 @pytest.mark.parametrize("pow2", [False, True])
 @pytest.mark.parametrize("N,K,trans", [(256, 512, True), (300, 384, True), (1, 128, True),
-                                       (130, 256, False), (7168, 7168, True)])
+                                       (130, 256, False), (7168, 7168, True),
+                                       (2048, 7168, True), (2000, 4096, True)])
 def test_quant_weight(oracle, N, K, trans, pow2):
     w = _special_rows(synth.weight(N, K, seed=300 + N))
     q_ref, s_ref = oracle.quant_weight(w, pow2)
