@@ -386,14 +386,16 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 // dequantised with one FP32 multiply, x = fl32(decode(q) * s_row), exactly as a
 // BF16 input would be read.
 //  - Tiles of 128 tokens x 128 channels (one row-scale group), channel blocks
-//    fastest; the raw codes arrive by TMA in a three-deep ring, 128-byte
-//    swizzled (16-byte chunk k of token row r at chunk k ^ (r % 8)).
+//    fastest; the raw codes arrive by TMA in a two-deep ring, 128-byte
+//    swizzled (16-byte chunk k of token row r at chunk k ^ (r % 8)); three
+//    CTAs of 256 threads per SM.
 //  - Warp w owns channels 16w..16w+15.  Four byte-wise ldmatrix.trans give
 //    lane 4g + t the codes of tokens 32p + 16h + 4t + {0..3} (p = 0..3,
 //    h = 0..1) of channels g and g + 8, four tokens of one channel per
 //    register: the codes are transposed as bytes, and decoding, scaling, the
 //    channel max-abs (two shuffles) and the new codes all happen in registers
-//    in the transposed orientation.
+//    in the transposed orientation, channel g first, then g + 8 (so that 32
+//    FP32 values are live, not 64, and three CTAs fit an SM).
 //  - Each warp stages its 16 channel rows of new codes (128-byte swizzle,
 //    conflict-free 32-bit stores) and writes them with its own TMA store.
 //  - No CTA barrier in the loop: each warp keeps its own copy of the row
@@ -401,8 +403,8 @@ __global__ void __launch_bounds__(kTileThreads) quant_act_T_kernel(
 //    input stage refills it (a shared counter with acquire-release order).
 constexpr int kRqThreads = 256;
 constexpr int kRqWarps = kRqThreads / 32;
-constexpr int kRqStages = 3;
-constexpr int kRqCtasPerSm = 2;
+constexpr int kRqStages = 2;
+constexpr int kRqCtasPerSm = 3;
 constexpr uint32_t kRqTileBytes = 128 * 128;   // raw codes, 128-byte token rows
 constexpr uint32_t kRqStripBytes = 16 * 128;   // one warp's 16 rows of new codes
 template <bool kPow2>
@@ -511,52 +513,39 @@ __global__ void __launch_bounds__(kRqThreads, kRqCtasPerSm) requant_act_T_kernel
       phase ^= 1u;
     }
 
-    // decode and scale: x[2k], x[2k+1] are tokens {0,1} and {2,3} of r[k] as
-    // packed FP32 (one mul.rn.f32x2 by the pair of row scales)
-    uint64_t x[32];
-    float am0 = 0.0f, am1 = 0.0f;
+    const uint32_t stg = strip0 + sb * kRqStripBytes;
+    const float *srwc = srw;
+    sb ^= 1u;
+    if (lane == 0) bulk_wait_group_read<1>();  // this strip's store two tiles ago has read it
+    __syncwarp();
+    // one channel at a time (g, then g + 8): decode and scale, x[2ph], x[2ph+1]
+    // are tokens {0,1} and {2,3} of r[2ph + j] as packed FP32 (one
+    // mul.rn.f32x2 by the pair of row scales), then max-abs, scale and codes
 #pragma unroll
-    for (int ph = 0; ph < 8; ++ph) {
-      const ulonglong2 sp = *reinterpret_cast<const ulonglong2 *>(&srw[16 * ph + 4 * tq]);
+    for (int j = 0; j < 2; ++j) {
+      uint64_t x[16];
+      float am = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int ph = 0; ph < 8; ++ph) {
+        const ulonglong2 sp = *reinterpret_cast<const ulonglong2 *>(&srwc[16 * ph + 4 * tq]);
         const int k = 2 * ph + j;
         const uint32_t h01 = decode_e4m3x2(static_cast<uint16_t>(r[k] & 0xFFFFu));
         const uint32_t h23 = decode_e4m3x2(static_cast<uint16_t>(r[k] >> 16));
-        x[2 * k] = fmul2(pack_f32x2(f16_lo(h01), f16_hi(h01)), sp.x);
-        x[2 * k + 1] = fmul2(pack_f32x2(f16_lo(h23), f16_hi(h23)), sp.y);
-        const float2 a = unpack_f32x2(x[2 * k]), b = unpack_f32x2(x[2 * k + 1]);
-        const float m = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
-        if (j == 0)
-          am0 = fmaxf(am0, m);
-        else
-          am1 = fmaxf(am1, m);
+        x[2 * ph] = fmul2(pack_f32x2(f16_lo(h01), f16_hi(h01)), sp.x);
+        x[2 * ph + 1] = fmul2(pack_f32x2(f16_lo(h23), f16_hi(h23)), sp.y);
+        const float2 a = unpack_f32x2(x[2 * ph]), b = unpack_f32x2(x[2 * ph + 1]);
+        am = fmaxf(am, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))));
       }
-    }
-    sb ^= 1u;
-    am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, 1));
-    am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 1));
-    am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, 2));
-    am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 2));
-    // lanes tq < 2 take channel g's scale, tq >= 2 channel g + 8's; shuffles
-    // give every lane both inverses
-    float sc, inv;
-    group_scale(tq < 2 ? am0 : am1, kPow2, sc, inv);
-    if ((tq & 1) == 0) sT[static_cast<int64_t>(tbc) * ld_sT + cbc * 128u + 16 * warp + g + 4 * tq] = sc;
-    const float inv0 = __shfl_sync(0xffffffffu, inv, lane & ~3);
-    const float inv1 = __shfl_sync(0xffffffffu, inv, (lane & ~3) | 2);
-    const uint64_t iv[2] = {pack_f32x2(inv0, inv0), pack_f32x2(inv1, inv1)};
-
-    const uint32_t stg = strip0 + (sb ^ 1u) * kRqStripBytes;
-    if (lane == 0) bulk_wait_group_read<1>();  // this strip's store two tiles ago has read it
-    __syncwarp();
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      float sc, inv;
+      group_scale(am, kPow2, sc, inv);
+      if (tq == 0) sT[static_cast<int64_t>(tbc) * ld_sT + cbc * 128u + 16 * warp + g + 8 * j] = sc;
+      const uint64_t iv = pack_f32x2(inv, inv);
 #pragma unroll
-    for (int ph = 0; ph < 8; ++ph) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int k = 2 * ph + j;
-        const float2 a = unpack_f32x2(fmul2(x[2 * k], iv[j]));
-        const float2 b = unpack_f32x2(fmul2(x[2 * k + 1], iv[j]));
+      for (int ph = 0; ph < 8; ++ph) {
+        const float2 a = unpack_f32x2(fmul2(x[2 * ph], iv));
+        const float2 b = unpack_f32x2(fmul2(x[2 * ph + 1], iv));
         // channel row g + 8j, token chunk ph (bytes 16ph + 4tq), swizzled by row % 8 = g
         st_shared_u32(stg + static_cast<uint32_t>(g + 8 * j) * 128u +
                           ((static_cast<uint32_t>(ph) ^ static_cast<uint32_t>(g)) << 4) + 4u * tq,
