@@ -190,6 +190,63 @@ def test_requant_act_T_from_fp8_cache(oracle, T, C, pow2):
 
 
 @pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("T,C,rows", [(256, 200, False), (384, 256, True)])
+def test_quant_act_T_strided(oracle, T, C, rows, pow2):
+    # every operand a view of a wider buffer: x (ldx > C), qT (ldqT > T),
+    # sT (ld_sT > C) and, with the fused rows, q_rows (ldq > C) and s_rows
+    # (ld_s_rows > T); the padding must keep its sentinel
+    full = _special_rows(synth.activation(T, C + 64, seed=250 + C))
+    x = bf16_to_torch(full)[:, :C]
+    qT = torch.full((C, T + 32), 0xA5, dtype=torch.uint8, device="cuda")
+    sT = torch.full((T // 128, C + 24), -3.0, dtype=torch.float32, device="cuda")
+    kw = {}
+    if rows:
+        kw = dict(q_rows=torch.full((T, C + 48), 0x5A, dtype=torch.uint8, device="cuda")[:, :C],
+                  s_rows=torch.full((C // 128, T + 12), -5.0, dtype=torch.float32,
+                                    device="cuda")[:, :T])
+    out = B.fp8q_quant_act_T(x, scale_mode=_mode(pow2), with_rows=rows, qT=qT[:, :T],
+                             sT=sT[:, :C], **kw)
+    torch.cuda.synchronize()
+    xs = np.ascontiguousarray(full[:, :C])
+    qT_ref, sT_ref = oracle.quant_act_T(xs, pow2)
+    assert_bytes_equal(u8(out[0]), qT_ref, "transposed codes")
+    assert_scales_equal(f32(out[1]), sT_ref, "128x1 scales")
+    assert np.all(u8(qT)[:, T:] == 0xA5), "wrote past T in the transposed rows"
+    assert np.all(f32(sT)[:, C:] == -3.0), "wrote past C in the scale rows"
+    if rows:
+        q_ref, s_ref = oracle.quant_act(xs, pow2)
+        assert_bytes_equal(u8(out[2]), q_ref, "1x128 codes (fused)")
+        assert_scales_equal(f32(out[3]), s_ref, "1x128 scales (fused)")
+        qr = torch.as_strided(out[2], (T, C + 48), (C + 48, 1))
+        sr = torch.as_strided(out[3], (C // 128, T + 12), (T + 12, 1))
+        assert np.all(u8(qr)[:, C:] == 0x5A), "wrote past C in the fused code rows"
+        assert np.all(f32(sr)[:, T:] == -5.0), "wrote past T in the fused scale rows"
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_requant_act_T_strided(oracle, pow2):
+    # cached codes and row scales as views of wider buffers (ldq > C,
+    # ld_s_rows > T, not a multiple of 4), outputs likewise (ldqT > T,
+    # ld_sT > C); three 128-channel groups, three token blocks
+    T, C = 384, 384
+    x = _special_rows(synth.activation(T, C, seed=510))
+    q = torch.full((T, C + 32), 0x11, dtype=torch.uint8, device="cuda")[:, :C]
+    s = torch.full((C // 128, T + 13), -7.0, dtype=torch.float32, device="cuda")[:, :T]
+    B.fp8q_quant_act(bf16_to_torch(x), scale_mode=_mode(pow2), q=q, sa=s)
+    qT = torch.full((C, T + 48), 0x22, dtype=torch.uint8, device="cuda")
+    sT = torch.full((T // 128, C + 8), -9.0, dtype=torch.float32, device="cuda")
+    B.fp8q_requant_act_T(q, s, scale_mode=_mode(pow2), qT=qT[:, :T], sT=sT[:, :C])
+    torch.cuda.synchronize()
+    q_r, s_r = oracle.quant_act(x, pow2)
+    qT_ref, sT_ref = oracle.requant_act_T(q_r, s_r, pow2)
+    assert_bytes_equal(u8(q), q_r, "cached codes")
+    assert_bytes_equal(u8(qT[:, :T]), qT_ref, "requantised codes")
+    assert_scales_equal(f32(sT[:, :C]), sT_ref, "requantised scales")
+    assert np.all(u8(qT)[:, T:] == 0x22), "wrote past T in the requantised rows"
+    assert np.all(f32(sT)[:, C:] == -9.0), "wrote past C in the requantised scales"
+
+
+@pytest.mark.parametrize("pow2", [False, True])
 @pytest.mark.parametrize("M,K", [(1, 8), (63, 200), (256, 1024), (4096, 7168)])
 def test_quant_tensor(oracle, M, K, pow2):
     x = _special_rows(synth.activation(M, K, seed=600 + M)) if K >= 256 else \
