@@ -193,7 +193,9 @@ constexpr int kTileThreads = 512;
 // ------------------------------------------------------------------ 128x1
 // Persistent: each CTA walks 128-token x 128-channel tiles (channel blocks
 // fastest) with a two-deep ring of input tiles filled by TMA, so the next
-// tile streams in while this one is reduced and converted.
+// tile streams in while this one is reduced and converted.  There is no CTA
+// barrier in the loop: the last warp to finish reading an input buffer
+// refills it.
 //  - Input: two 64-channel halves per tile, 128-byte swizzled (the 16-byte
 //    chunk k of token row r sits at chunk k ^ (r % 8)), so that ldmatrix.trans
 //    reads 8 consecutive token rows of one chunk without bank conflicts.
@@ -202,11 +204,13 @@ constexpr int kTileThreads = 512;
 //    m = 0..15).  The channel's max-abs is a packed max over them and two
 //    shuffles; no other warp is involved.
 //  - Codes go to a swizzled shared-memory copy of the transposed tile
-//    (channel rows of 128 bytes) that one TMA store writes out, so the
-//    transposed output costs no per-thread global stores.
+//    (channel rows of 128 bytes); each warp writes its 8 rows (1 KB) with its
+//    own TMA store, so the transposed output costs no per-thread global
+//    stores and no CTA barrier.
 //  - Optionally the 1x128 codes of each token row (eight lanes per row, 32
 //    bytes each).
-// Channels past C are zero-filled by TMA and clipped by the TMA store.
+// Channels past C are zero-filled by TMA; a warp whose 8 channel rows lie
+// past C (C % 8 == 0: all of them or none) issues no store.
 constexpr uint32_t kTileBytesBF16 = 128 * 128 * 2;
 constexpr uint32_t kHalfBytesBF16 = kTileBytesBF16 / 2;   // 128 tokens x 64 channels
 constexpr uint32_t kTileBytesQ = 128 * 128;                // one 128 x 128 tile of E4M3 codes
