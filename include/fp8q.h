@@ -92,7 +92,8 @@ fp8q_status fp8q_quant_act(const void *x, int64_t M, int64_t K, int64_t ldx,
  * column (channel) c per 128 rows (tokens) ([dssusan] paragraph 4: 1x128
  * tiles become 128x1 tiles).  The codes are written TRANSPOSED so the token
  * dimension is contiguous, i.e. K-major for the Wgrad GEMM.
- *   x      BF16 [T][ldx], columns [0, C).           T % 128 == 0, C % 8 == 0.
+ *   x      BF16 [T][ldx], columns [0, C).           T % 128 == 0, C % 8 == 0,
+ *          T <= 65535 * 128, C <= 2^31 - 128 (else FP8Q_ERR_SHAPE).
  *   qT     E4M3 [C][ldqT], qT[c][t] = code of x[t][c].
  *   sT     FP32, scale of (t-group tg, c) at sT[tg * ld_sT + c], ld_sT >= C.
  *   q_rows optional (NULL to skip): the 1x128 quantisation of the same x,

@@ -51,6 +51,24 @@ def test_host_only_calls(lib):
     assert lib.fp8q_quant_act(None, 0, 128, 128, None, 128, None, 0, 0, None) == binding.FP8Q_OK
 
 
+def test_tile_coordinate_limits_checked_on_the_host(lib):
+    # the persistent quantisers step 32-bit tile coordinates: shapes past that
+    # range are rejected before any pointer or device is touched
+    from fp8_fine_grained_amax_gb300 import binding
+    big = 1 << 31  # a multiple of 128 just past INT32_MAX
+    assert lib.fp8q_requant_act_T(None, 128, big, big, None, 128, None, 128, None, big, 0,
+                                  None) == binding.FP8Q_ERR_SHAPE
+    assert lib.fp8q_requant_act_T(None, 128 * 65536, 128, 128, None, 128 * 65536, None,
+                                  128 * 65536, None, 128, 0, None) == binding.FP8Q_ERR_SHAPE
+    assert lib.fp8q_quant_act_T(None, 128, big, big, None, 128, None, big, None, 0, None, 0, 0,
+                                None) == binding.FP8Q_ERR_SHAPE
+    # one size smaller gets past the shape checks (to the pointer checks)
+    assert lib.fp8q_requant_act_T(None, 128, big - 128, big - 128, None, 128, None, 128, None,
+                                  big - 128, 0, None) == binding.FP8Q_ERR_INVALID
+    assert lib.fp8q_quant_act_T(None, 128, big - 128, big - 128, None, 128, None, big - 128, None,
+                                0, None, 0, 0, None) == binding.FP8Q_ERR_INVALID
+
+
 def test_package_has_no_cpu_path():
     # the product package must not import the oracle
     pkg = os.path.join(ROOT, "fp8_fine_grained_amax_gb300")
