@@ -308,3 +308,40 @@ def test_gemm_accumulate_block_scales(oracle, kind):
     # the product's bound, plus the one FP32 rounding of the addition
     tol = 2e-4 * ad + np.abs(ref) * 2.0 ** -24 + 1e-30
     assert_within_tolerance(f64(c), ref, tol, f"accumulate {kind}")
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("kind", ["fprop", "wgrad"])
+def test_gemm_deep_k(oracle, kind, pow2):
+    # K = 16384: 128 K-groups through the FP32 fold (both TMEM buffers cycle
+    # 64 times) or through the power-of-two kernel's scale ring; Wgrad reduces
+    # over 16384 tokens (per-column scales, FP32 out)
+    mode = B.FP8Q_SCALE_POW2 if pow2 else B.FP8Q_SCALE_FP32
+    gemm = B.fp8q_gemm_pow2 if pow2 else B.fp8q_gemm
+    K = 16384
+    if kind == "fprop":
+        M, N = 200, 256
+        x = synth.activation(M, K, seed=91, name="deepk.X")
+        w = synth.weight(N, K, seed=92, name="deepk.W")
+        qa, sa = B.fp8q_quant_act(bf16_to_torch(x), scale_mode=mode)
+        qb, sb = B.fp8q_quant_weight(bf16_to_torch(w), scale_mode=mode)
+        c = gemm(qa, sa, qb, sb)
+        qa_r, sa_r = oracle.quant_act(x, pow2)
+        qb_r, sb_r = oracle.quant_weight(w, pow2)
+        bk, bf16_out = oracle.BSCALE_BLOCK, True
+    else:
+        M, N = 256, 136
+        dy = synth.normal_bf16((K, M), 1e-3, 93, "deepk.dY")
+        xx = synth.activation(K, N, seed=94, name="deepk.Xw")
+        qa, sa = B.fp8q_quant_act_T(bf16_to_torch(dy), scale_mode=mode)
+        qb, sb = B.fp8q_quant_act_T(bf16_to_torch(xx), scale_mode=mode)
+        c = gemm(qa, sa, qb, sb, bscale_kind=B.FP8Q_BSCALE_ROW, out_dtype=B.FP8Q_OUT_FP32)
+        qa_r, sa_r = oracle.quant_act_T(dy, pow2)
+        qb_r, sb_r = oracle.quant_act_T(xx, pow2)
+        bk, bf16_out = oracle.BSCALE_ROW, False
+    torch.cuda.synchronize()
+    assert_bytes_equal(u8(qa), qa_r, "A codes")
+    assert_bytes_equal(u8(qb), qb_r, "B codes")
+    ref, ad = oracle.gemm_rows(qa_r, sa_r, qb_r, sb_r, bk)
+    assert_within_tolerance(f64(c), ref, oracle.gemm_tolerance(ref, ad, bf16_out),
+                            f"{kind} K={K}")
