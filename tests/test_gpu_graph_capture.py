@@ -1,5 +1,6 @@
-"""Every entry point inside a CUDA graph: one replay of the captured call writes
-the same bytes as the same call run eagerly.  The library keeps no host state
+"""Every entry point inside a CUDA graph, and independent calls on two streams
+at once: one replay of the captured call writes the same bytes as the same
+call run eagerly, and concurrent chains write what they write alone.  The library keeps no host state
 that a graph would freeze: tensor maps and arguments travel by value in the
 kernel parameters, and the stream is the caller's (here the capture stream).
 Outputs are preallocated, so nothing is allocated while capturing.
@@ -125,3 +126,39 @@ def test_grouped_gemm_in_a_graph(pow2):
         B.fp8q_quant_weight(wg, scale_mode=mode, q=qb[g], sb=sb[g])
     _eager_vs_graph(lambda o: grouped(qa, sa, qb, sb, offs, c=o[0]),
                     lambda: (_empty((M, Ne), BF),))
+
+
+def test_independent_calls_on_two_streams():
+    # two chains of calls on two streams with no dependency between them run
+    # concurrently on the GPU; each must write exactly what it writes alone
+    # (the library keeps no shared device state besides the error words and
+    # the documented scratch of fp8q_quant_tensor_noalloc, not used here)
+    x = bf16_to_torch(synth.activation(2048, 1024, seed=81, name="streams.X"))
+    w = bf16_to_torch(synth.weight(1024, 1024, seed=82, name="streams.W"))
+    dy = bf16_to_torch(synth.normal_bf16((2048, 1024), 1e-3, 83, "streams.dY"))
+    q, s = B.fp8q_quant_act(x)
+    torch.cuda.synchronize()
+
+    def chain_a(st):
+        qT, sT = B.fp8q_requant_act_T(q, s, stream=st)
+        out = B.fp8q_quant_act_T(dy, with_rows=True, stream=st)
+        _, sbw, qwT = B.fp8q_quant_weight(w, with_transpose=True, stream=st)
+        dx = B.fp8q_gemm(out[2], out[3], qwT, sbw, bscale_kind=B.FP8Q_BSCALE_BLOCK_T, stream=st)
+        return [qT, sT, *out, dx]
+
+    def chain_b(st):
+        qb, sb = B.fp8q_quant_weight(w, stream=st)
+        y = B.fp8q_gemm(q, s, qb, sb, stream=st)
+        return [qb, sb, y]
+
+    ref = chain_a(torch.cuda.current_stream()) + chain_b(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    sa_, sb_ = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        sa_.wait_stream(torch.cuda.current_stream())
+        sb_.wait_stream(torch.cuda.current_stream())
+        got = chain_a(sa_) + chain_b(sb_)
+        torch.cuda.synchronize()
+        assert B.fp8q_sync_status() == 0
+        for i, (a, b) in enumerate(zip(ref, got)):
+            assert np.array_equal(_bytes(a), _bytes(b)), f"output {i} differs when run concurrently"
